@@ -1,0 +1,141 @@
+"""CPU oracle for the scaled FP8 / BF16 GEMM -- TEST INFRASTRUCTURE ONLY.
+
+Only tests/, ``__graft_entry__.smoke()`` and bench.py's CPU-baseline and
+reference arms may import this package.  It wraps ``oracle.c`` (plain C,
+binary64 accumulation, exact e4m3 / e8m0 / bf16 decoders) through ctypes and
+shares no code with the CUDA library.  See oracle.c for the definition it
+computes and the passages it follows.
+
+Array conventions (numpy, C-contiguous):
+  A  [M, K] uint8 e4m3fn codes (uint16 bf16 bits in bf16 mode)
+  B  [N, K] same type as A
+  ptpc        sa float32 [M],        sb float32 [N]
+  blockscale  sa float32 [K/128, M], sb float32 [ceil(N/128), K/128]
+  mxfp8       sa uint8   [K/32, M],  sb uint8   [K/32, N]   (e8m0 codes)
+  bf16        sa = sb = None
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+MODES = {"bf16": 0, "ptpc": 1, "blockscale": 2, "mxfp8": 3}
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.sgo_dec_e4m3.restype = ctypes.c_double
+        L.sgo_dec_e4m3.argtypes = [ctypes.c_uint8]
+        L.sgo_dec_e8m0.restype = ctypes.c_double
+        L.sgo_dec_e8m0.argtypes = [ctypes.c_uint8]
+        L.sgo_dec_bf16.restype = ctypes.c_double
+        L.sgo_dec_bf16.argtypes = [ctypes.c_uint16]
+        L.sgo_bf16_rne.restype = ctypes.c_uint16
+        L.sgo_bf16_rne.argtypes = [ctypes.c_double]
+        i64 = ctypes.c_int64
+        vp = ctypes.c_void_p
+        L.sgo_gemm_rows.restype = ctypes.c_int
+        L.sgo_gemm_rows.argtypes = [ctypes.c_int, i64, i64, i64, vp, vp, vp, vp, i64, i64, vp, vp]
+        L.sgo_gemm_points.restype = ctypes.c_int
+        L.sgo_gemm_points.argtypes = [ctypes.c_int, i64, i64, i64, vp, vp, vp, vp, i64, vp, vp, vp, vp]
+        L.sgo_num_threads.restype = ctypes.c_int
+        L.sgo_num_threads.argtypes = []
+        _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's GEMM loops use."""
+    return int(lib().sgo_num_threads())
+
+
+def dec_e4m3(codes) -> np.ndarray:
+    L = lib()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.sgo_dec_e4m3(int(b)) for b in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def dec_e8m0(codes) -> np.ndarray:
+    L = lib()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([L.sgo_dec_e8m0(int(b)) for b in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def dec_bf16(bits) -> np.ndarray:
+    L = lib()
+    c = np.asarray(bits, dtype=np.uint16)
+    return np.array([L.sgo_dec_bf16(int(b)) for b in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def bf16_rne(x) -> np.ndarray:
+    """Round binary64 values to bf16 bits (uint16), nearest-even, in one step."""
+    L = lib()
+    v = np.asarray(x, dtype=np.float64)
+    return np.array([L.sgo_bf16_rne(float(t)) for t in v.ravel()], dtype=np.uint16).reshape(v.shape)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _prep(mode, A, B, sa, sb):
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    dt = np.uint16 if m == 0 else np.uint8
+    A = np.ascontiguousarray(A).view(dt)
+    B = np.ascontiguousarray(B).view(dt)
+    if m == 0:
+        sa = sb = None
+    elif m == 3:
+        sa = np.ascontiguousarray(sa, dtype=np.uint8)
+        sb = np.ascontiguousarray(sb, dtype=np.uint8)
+    else:
+        sa = np.ascontiguousarray(sa, dtype=np.float32)
+        sb = np.ascontiguousarray(sb, dtype=np.float32)
+    return m, A, B, sa, sb
+
+
+def gemm(mode, A, B, sa, sb, rows=None, want_r=True):
+    """Rows ``rows=(m0, m1)`` (default all) of the result.
+
+    Returns ``(R, ref)``: R float64 [rows, N] (None unless ``want_r``) and
+    ref uint16 bf16 bits [rows, N].
+    """
+    m, A, B, sa, sb = _prep(mode, A, B, sa, sb)
+    M, K = A.shape
+    N = B.shape[0]
+    assert B.shape[1] == K
+    m0, m1 = (0, M) if rows is None else rows
+    R = np.empty((m1 - m0, N), dtype=np.float64) if want_r else None
+    ref = np.empty((m1 - m0, N), dtype=np.uint16)
+    rc = lib().sgo_gemm_rows(m, M, N, K, _ptr(A), _ptr(B), _ptr(sa), _ptr(sb), m0, m1, _ptr(R), _ptr(ref))
+    if rc != 0:
+        raise ValueError("oracle gemm rejected its arguments (rc=%d)" % rc)
+    return R, ref
+
+
+def gemm_points(mode, A, B, sa, sb, ms, ns):
+    """Elements (ms[i], ns[i]) computed one by one: returns (R float64, ref uint16)."""
+    m, A, B, sa, sb = _prep(mode, A, B, sa, sb)
+    M, K = A.shape
+    N = B.shape[0]
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    R = np.empty(ms.shape[0], dtype=np.float64)
+    ref = np.empty(ms.shape[0], dtype=np.uint16)
+    rc = lib().sgo_gemm_points(m, M, N, K, _ptr(A), _ptr(B), _ptr(sa), _ptr(sb), ms.shape[0], _ptr(ms), _ptr(ns), _ptr(R), _ptr(ref))
+    if rc != 0:
+        raise ValueError("oracle gemm_points rejected its arguments (rc=%d)" % rc)
+    return R, ref
+
+
+def bits_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64 values, via the oracle's own decoder rule."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)

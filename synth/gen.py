@@ -1,0 +1,183 @@
+"""Input generation for the scaled GEMM: seeded normals, quantised to e4m3.
+
+The recipe (the pages give shapes and distributions, not values):
+  * one ``torch.Generator('cpu')`` per case, seeded with the case's seed; A is
+    drawn first, then B, as float32 ``randn`` times the case's standard
+    deviation (N(0,1) for A, N(0,1) or N(0,0.02) for B);
+  * ptpc:        A quantised per row (per token), B per output row (per
+    channel), scale = amax / 448, codes = RNE(x / scale) clamped to +-448;
+  * blockscale:  A per 1x128 block along K, B per 128x128 block, fp32 scales,
+    same rule;
+  * mxfp8:       per 32 consecutive K elements of a row, scale 2^e with
+    e = ceil(log2(amax / 448)) stored as e8m0 code e + 127 (clamped to 0..254);
+  * an all-zero row / block gets scale 1.0 (e8m0 127);
+  * bf16:        randn rounded to bf16 (RNE).
+Scale layouts: ptpc sa [M], sb [N]; blockscale sa [K/128, M] (K-block major),
+sb [ceil(N/128), K/128]; mxfp8 sa [K/32, M], sb [K/32, N] (K-block major).
+"""
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+E4M3_MAX = 448.0
+
+
+@dataclasses.dataclass
+class Case:
+    """One GEMM problem.  Tensors are CPU torch tensors.
+
+    A, B:  uint8 e4m3 codes [M,K] / [N,K] (bf16 mode: torch.bfloat16)
+    sa, sb: scales in the layout of the mode (None for bf16)
+    """
+
+    mode: str
+    M: int
+    N: int
+    K: int
+    A: torch.Tensor
+    B: torch.Tensor
+    sa: Optional[torch.Tensor]
+    sb: Optional[torch.Tensor]
+    seed: int = 0
+
+    def numpy(self):
+        """(A, B, sa, sb) as numpy arrays in the oracle's conventions."""
+        if self.mode == "bf16":
+            A = self.A.view(torch.int16).numpy().view(np.uint16)
+            B = self.B.view(torch.int16).numpy().view(np.uint16)
+            return A, B, None, None
+        return self.A.numpy(), self.B.numpy(), self.sa.numpy(), self.sb.numpy()
+
+    @property
+    def flops(self) -> float:
+        return gemm_flops(self.M, self.N, self.K)
+
+
+def _to_e4m3_codes(x: torch.Tensor) -> torch.Tensor:
+    return x.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _safe_scale(amax: torch.Tensor) -> torch.Tensor:
+    s = amax / E4M3_MAX
+    return torch.where(amax > 0, s, torch.ones_like(s))
+
+
+def quantize_e4m3_rows(x: torch.Tensor):
+    """Per-row amax/448 quantisation: returns (codes uint8 [R,C], scale fp32 [R])."""
+    x = x.float()
+    s = _safe_scale(x.abs().amax(dim=1))
+    return _to_e4m3_codes(x / s[:, None]), s.contiguous()
+
+
+def quantize_e4m3_blocks_1x128(x: torch.Tensor):
+    """A-side blockscale: one scale per row per 128 K.  Returns codes, scale [K/128, M]."""
+    R, C = x.shape
+    assert C % 128 == 0
+    xb = x.float().reshape(R, C // 128, 128)
+    s = _safe_scale(xb.abs().amax(dim=2))  # [R, K/128]
+    q = _to_e4m3_codes(xb / s[:, :, None]).reshape(R, C)
+    return q, s.t().contiguous()
+
+
+def quantize_e4m3_blocks_128x128(w: torch.Tensor):
+    """B-side blockscale: one scale per 128x128 block.  Returns codes, scale [ceil(N/128), K/128]."""
+    N, K = w.shape
+    assert K % 128 == 0
+    nb = (N + 127) // 128
+    wp = torch.zeros(nb * 128, K, dtype=torch.float32)
+    wp[:N] = w.float()
+    wb = wp.reshape(nb, 128, K // 128, 128)
+    s = _safe_scale(wb.abs().amax(dim=(1, 3)))  # [nb, K/128]
+    q = _to_e4m3_codes(wb / s[:, None, :, None]).reshape(nb * 128, K)[:N]
+    return q.contiguous(), s.contiguous()
+
+
+def quantize_mx_rows(x: torch.Tensor):
+    """MX quantisation per 32 K elements of each row.  Returns codes, e8m0 codes [K/32, R]."""
+    R, C = x.shape
+    assert C % 32 == 0
+    xb = x.float().reshape(R, C // 32, 32)
+    amax = xb.abs().amax(dim=2).double()
+    e = torch.ceil(torch.log2(amax / E4M3_MAX))
+    e = torch.where(amax > 0, e, torch.zeros_like(e))
+    code = (e + 127).clamp(0, 254)
+    scale = torch.pow(2.0, code - 127).float()
+    q = _to_e4m3_codes(xb / scale[:, :, None]).reshape(R, C)
+    return q, code.to(torch.uint8).t().contiguous()
+
+
+def _draw(gen, rows, cols, std):
+    return torch.randn(rows, cols, generator=gen, dtype=torch.float32) * std
+
+
+def make_case(mode: str, M: int, N: int, K: int, seed: int = 0, a_std: float = 1.0, b_std: float = 1.0) -> Case:
+    """Seeded synthetic case in the given scale mode (A drawn first, then B)."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    a = _draw(g, M, K, a_std)
+    b = _draw(g, N, K, b_std)
+    if mode == "bf16":
+        return Case(mode, M, N, K, a.bfloat16().contiguous(), b.bfloat16().contiguous(), None, None, seed)
+    if mode == "ptpc":
+        qa, sa = quantize_e4m3_rows(a)
+        qb, sb = quantize_e4m3_rows(b)
+    elif mode == "blockscale":
+        qa, sa = quantize_e4m3_blocks_1x128(a)
+        qb, sb = quantize_e4m3_blocks_128x128(b)
+    elif mode == "mxfp8":
+        qa, sa = quantize_mx_rows(a)
+        qb, sb = quantize_mx_rows(b)
+    else:
+        raise ValueError("unknown mode %r" % mode)
+    return Case(mode, M, N, K, qa.contiguous(), qb.contiguous(), sa, sb, seed)
+
+
+def make_int_case(M: int, N: int, K: int, lo: int = -16, hi: int = 16, seed: int = 0) -> Case:
+    """ptpc case with integer-valued e4m3 operands in [lo, hi] and unit scales."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    a = torch.randint(lo, hi + 1, (M, K), generator=g).float()
+    b = torch.randint(lo, hi + 1, (N, K), generator=g).float()
+    return Case(
+        "ptpc", M, N, K, _to_e4m3_codes(a), _to_e4m3_codes(b),
+        torch.ones(M, dtype=torch.float32), torch.ones(N, dtype=torch.float32), seed,
+    )
+
+
+def gemm_flops(M, N, K) -> float:
+    return 2.0 * M * N * K
+
+
+def gemm_bytes(mode, M, N, K) -> float:
+    """Algorithmic bytes of one GEMM: operands once, C once, scales once."""
+    el = 2 if mode == "bf16" else 1
+    b = el * (M * K + N * K) + 2 * M * N
+    if mode == "ptpc":
+        b += 4 * (M + N)
+    elif mode == "blockscale":
+        b += 4 * (M * (K // 128) + math.ceil(N / 128) * (K // 128))
+    elif mode == "mxfp8":
+        b += (M + N) * (K // 32)
+    return float(b)
+
+
+# The five workloads, as (name, mode, M, N, K, seed, a_std, b_std).
+CONFIGS = {
+    "c0_ptpc_256x512x256": ("ptpc", 256, 512, 256, 0, 1.0, 1.0),
+    "c1_ptpc_4096x7168x256": ("ptpc", 4096, 7168, 256, 0, 1.0, 1.0),
+    "c2_ptpc_16384x7168x512": ("ptpc", 16384, 7168, 512, 0, 1.0, 0.02),
+    "c2_ptpc_32768x7168x1792": ("ptpc", 32768, 7168, 1792, 0, 1.0, 0.02),
+    "c3_blockscale_16384x7168x2048": ("blockscale", 16384, 7168, 2048, 0, 1.0, 0.02),
+    "c3_mxfp8_32768x7168x1792": ("mxfp8", 32768, 7168, 1792, 0, 1.0, 0.02),
+    "c4_ptpc_32768x6288x7168": ("ptpc", 32768, 6288, 7168, 0, 1.0, 0.02),
+    "c4_ptpc_32768x3648x7168": ("ptpc", 32768, 3648, 7168, 0, 1.0, 0.02),
+    "c4_ptpc_32768x6400x7168": ("ptpc", 32768, 6400, 7168, 0, 1.0, 0.02),
+    "c4_bf16_4096x896x1024": ("bf16", 4096, 896, 1024, 233, 1.0, 1.0),
+}
+
+# One benchmark step runs each of these once (every M x 7168 x K shape, all
+# three scale modes, the unpadded-N shapes and the BF16 GEMM).
+SUITE = [k for k in CONFIGS if not k.startswith("c0_")]
