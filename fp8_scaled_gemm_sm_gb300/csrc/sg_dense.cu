@@ -1,0 +1,314 @@
+// sg_dense.cu -- persistent warp-specialised GEMM for the ptpc and bf16 modes.
+//
+//   C[m,n] = bf16(acc[m,n] * a_scale[m] * b_scale[n])   (ptpc, e4m3 x e4m3)
+//   C[m,n] = bf16(acc[m,n])                             (bf16 x bf16)
+//
+// Per CTA (one per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: waits empty[s], arms full[s] with the stage's byte
+//               count and loads the A tile [128 x 128 B] and B tile [BN x 128 B]
+//               (128-byte swizzle) into stage s of the shared-memory ring.
+//   warp 1      allocates TMEM (two BN-column fp32 accumulators); one thread
+//               waits full[s], issues 4 tcgen05.mma (K = 32 fp8 / 16 bf16 each)
+//               and commits to empty[s], so a stage is handed back only after
+//               the tensor core has finished reading it; after a tile's last K
+//               block it commits to tmem_full[acc].
+//   warps 2..   epilogue: wait tmem_full[acc], read the accumulator with
+//               tcgen05.ld, scale, round to bf16, stage in shared memory, fence
+//               the async proxy, store by TMA; release the accumulator with
+//               tcgen05.fence::before_thread_sync + arrive on tmem_empty[acc].
+//
+// The stage / phase counters run continuously across tiles, so a K loop of one
+// or two blocks (the "peeled tail" case, K <= 256) goes through exactly the
+// same waits as a long one: no read of a stage happens before the wait on the
+// barrier that its producer's bytes complete (ROCm/mori PR 785, Problem and
+// Fix; ROCm/aiter PR 6539, Technical Details).  Stages are released only by
+// tcgen05.commit, which fires after the MMAs that read them
+// (deepseek-ai/DeepGEMM PR 453, ds-review-bot v4: "release smem only after
+// UMMA commits").  The epilogue's generic shared-memory writes are fenced into
+// the async proxy by every writing thread before the TMA store is issued
+// (deepseek-ai/DeepGEMM PR 453, Fix).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sg_common.cuh"
+#include "sg_internal.h"
+
+namespace sg {
+
+template <int BN, int STAGES, int EPI_WARPS>
+struct DenseLayout {
+  static constexpr int kAStage = kBM * kRowBytes;
+  static constexpr int kBStage = BN * kRowBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + STAGES * kAStage;
+  static constexpr int kOffC = kOffB + STAGES * kBStage;
+  static constexpr int kOffScale = kOffC + EPI_WARPS * 2 * kCBoxBytes;  // per-warp column scales
+  static constexpr int kScaleCols = BN * 4 / EPI_WARPS;                   // columns per warp
+  static constexpr int kOffBar = kOffScale + EPI_WARPS * kScaleCols * 4;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16 + 4 * STAGES;
+  static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kOffC % 1024 == 0, "store boxes need 512-byte alignment");
+};
+
+template <int MODE, int BN, int STAGES, int EPI_WARPS>
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
+    dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  using L = DenseLayout<BN, STAGES, EPI_WARPS>;
+  constexpr bool kScaled = (MODE == kModePtpc);
+  constexpr int kBK = (MODE == kModeBf16) ? 64 : 128;       // K elements per stage
+  constexpr int kUmmaK = (MODE == kModeBf16) ? 16 : 32;      // K per tcgen05.mma
+  constexpr int kKSteps = kBK / kUmmaK;
+  constexpr uint32_t kIdesc =
+      (MODE == kModeBf16) ? instr_desc(1, 1, kBM, BN) : instr_desc(0, 0, kBM, BN);
+  constexpr uint32_t kTx = L::kAStage + L::kBStage;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr int kAccStride = 256;
+  constexpr int kColsPerWarp = BN * 4 / EPI_WARPS;
+  static_assert(BN <= 256 && BN % 64 == 0, "BN");
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA = smem_addr(smem + L::kOffA);
+  const uint32_t sB = smem_addr(smem + L::kOffB);
+  const uint32_t sC = smem_addr(smem + L::kOffC);
+  const uint32_t bar0 = smem_addr(smem + L::kOffBar);
+  auto full_bar = [&](int s) { return bar0 + 8 * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8 * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  uint32_t* last_par = misc + 4;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 32 * EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    misc[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0, kstep = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord(p, t);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (kstep != p.skip_kstep) {
+            mbar_arrive_expect_tx(full_bar(stage), kTx);
+            tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
+            tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN, full_bar(stage));
+            issued |= 1u << stage;
+            last_par[stage] = phase;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {  // loads still in flight must land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccStride;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, wd, kWhereMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sA + stage * L::kAStage;
+          const uint32_t b0 = sB + stage * L::kBStage;
+#pragma unroll
+          for (int k = 0; k < kKSteps; ++k) {
+            const uint64_t ad = kmajor_sw128_desc(a0 + k * kUmmaK * (kRowBytes / kBK));
+            const uint64_t bd = kmajor_sw128_desc(b0 + k * kUmmaK * (kRowBytes / kBK));
+            if constexpr (MODE == kModeBf16)
+              mma_f16(d, ad, bd, kIdesc, (kb | k) != 0);
+            else
+              mma_f8f6f4(d, ad, bd, kIdesc, (kb | k) != 0);
+          }
+          mma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+      }
+      if (!ok) {  // let issued MMAs finish before TMEM is freed
+        mma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 2;          // 0 .. EPI_WARPS-1
+    const int quarter = warp & 3;     // TMEM lanes this warp may access
+    const int col0 = (ew >> 2) * kColsPerWarp;
+    const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
+    float* col_scale = reinterpret_cast<float*>(smem + L::kOffScale) + ew * kColsPerWarp;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      const TileCoord tc = tile_coord(p, t);
+      const int acc = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      const int m_start = tc.mb * kBM + quarter * 32;
+      const int n_start = tc.nb * BN + col0;
+      float row_scale = 0.f;
+      if constexpr (kScaled) {
+        __syncwarp();
+        for (int i = lane; i < kColsPerWarp; i += 32) {
+          const int n = n_start + i;
+          col_scale[i] = (n < p.N) ? p.b_scale[n] : 0.f;
+        }
+        const int row = m_start + lane;
+        row_scale = (row < p.M) ? p.a_scale[row] : 0.f;
+        __syncwarp();
+      }
+      const bool ok = mbar_wait(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             acc * kAccStride + col0;
+      epilogue_tile<kColsPerWarp, kScaled>(taddr, bufs, col_scale, row_scale, &tmC, n_start,
+                                          m_start, p.N, p.M, lane, [&]() {
+                                            tc_fence_before();
+                                            mbar_arrive(tempty_bar(acc));
+                                          });
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+namespace {
+
+constexpr int kDenseBN = 256;
+constexpr int kDenseStages = 4;
+constexpr int kDenseEpiWarps = 4;
+
+template <int MODE>
+struct DenseKernel {
+  using L = DenseLayout<kDenseBN, kDenseStages, kDenseEpiWarps>;
+  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, kDenseStages, kDenseEpiWarps>;
+  static constexpr int kThreads = 64 + 32 * kDenseEpiWarps;
+};
+
+template <int MODE>
+cudaError_t prepare_dense() {
+  return cudaFuncSetAttribute(DenseKernel<MODE>::fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DenseKernel<MODE>::L::kDynSmem);
+}
+
+template <int MODE>
+sg_status_t launch_dense_impl(const LaunchArgs& a) {
+  using K = DenseKernel<MODE>;
+  const bool bf16 = (MODE == kModeBf16);
+  const int bk = bf16 ? 64 : 128;
+  const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint64_t el = bf16 ? 2 : 1;
+  CUtensorMap tmA, tmB, tmC;
+  if (!encode_2d(&tmA, dt, a.A, a.K, a.M, a.K * el, bk, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, kDenseBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols,
+                 kCBoxRows, CU_TENSOR_MAP_SWIZZLE_64B))
+    return SG_ERR_CUDA;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(a.M);
+  p.N = static_cast<int32_t>(a.N);
+  p.K = static_cast<int32_t>(a.K);
+  p.m_blocks = static_cast<int32_t>((a.M + kBM - 1) / kBM);
+  p.n_blocks = static_cast<int32_t>((a.N + kDenseBN - 1) / kDenseBN);
+  p.k_blocks = static_cast<int32_t>((a.K + bk - 1) / bk);
+  p.num_tiles = p.m_blocks * p.n_blocks;
+  p.skip_kstep = a.skip_kstep;
+  p.a_scale = static_cast<const float*>(a.a_scale);
+  p.b_scale = static_cast<const float*>(a.b_scale);
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
+  K::fn<<<grid, K::kThreads, K::L::kDynSmem, a.stream>>>(tmA, tmB, tmC, p);
+  return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
+}
+
+}  // namespace
+
+cudaError_t dense_prepare(int mode) {
+  return mode == kModeBf16 ? prepare_dense<kModeBf16>() : prepare_dense<kModePtpc>();
+}
+
+sg_status_t dense_launch(const LaunchArgs& a) {
+  return a.mode == kModeBf16 ? launch_dense_impl<kModeBf16>(a) : launch_dense_impl<kModePtpc>(a);
+}
+
+void dense_config(int mode, TileConfig* c) {
+  c->bm = kBM;
+  c->bn = kDenseBN;
+  c->bk = mode == kModeBf16 ? 64 : 128;
+  c->stages = kDenseStages;
+}
+
+}  // namespace sg

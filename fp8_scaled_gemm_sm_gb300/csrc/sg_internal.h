@@ -1,0 +1,51 @@
+// sg_internal.h -- host-side interface between the C ABI (scaled_gemm.cu) and
+// the per-mode kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "scaled_gemm.h"
+
+namespace sg {
+
+// Everything one launch needs, validated by the C ABI before any launcher runs.
+struct LaunchArgs {
+  int mode;
+  int64_t M, N, K;
+  const void* A;
+  const void* B;
+  const void* a_scale;
+  const void* b_scale;
+  void* C;
+  cudaStream_t stream;
+  int num_sms;
+  int* status;          // device status word of the plan
+  uint64_t timeout_ns;  // per-wait limit
+  int32_t skip_kstep;   // watchdog tests: -1 = off
+};
+
+struct TileConfig {
+  int bm, bn, bk, stages;
+};
+
+// Encode a 2D tiled TMA descriptor (inner dimension first).  Returns false if
+// the driver rejects it.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle);
+
+cudaError_t dense_prepare(int mode);
+sg_status_t dense_launch(const LaunchArgs& a);
+void dense_config(int mode, TileConfig* c);
+
+cudaError_t mxfp8_prepare();
+sg_status_t mxfp8_launch(const LaunchArgs& a);
+void mxfp8_config(TileConfig* c);
+
+cudaError_t blockscale_prepare();
+sg_status_t blockscale_launch(const LaunchArgs& a);
+void blockscale_config(TileConfig* c);
+
+}  // namespace sg

@@ -1,0 +1,132 @@
+/*
+ * scaled_gemm.h -- C ABI of the GB300 (sm_103a) scaled FP8 / BF16 GEMM library
+ * (libscaledgemm.so).
+ *
+ * The operation (one launch):
+ *
+ *     C[M,N] = bf16( (A[M,K] . B[N,K]^T) (.) scales ),   fp32 accumulation,
+ *
+ * in one of four modes:
+ *
+ *   SG_MODE_PTPC        per-token x per-channel:  C = bf16(acc[m,n] * a_scale[m] * b_scale[n]).
+ *                       ROCm/mori PR 809, "Using it" (A [M,K] fp8 with a per-row scale from
+ *                       quantize_per_token, the weight shard B [N,K] with its scale,
+ *                       bf16 [M,N] out); ROCm/mori PR 785 cost table ("ptpc").
+ *   SG_MODE_BLOCKSCALE  fp32 scales per 1x128 block of A and per 128x128 block of B:
+ *                       C = bf16( sum_j acc_j[m,n] * a_scale[j][m] * b_scale[n/128][j] ),
+ *                       acc_j the fp32 partial over K block j.  ROCm/mori PR 785 cost table
+ *                       ("blockscale"); PR 809 "Not done yet" (the A scale is K-block major).
+ *   SG_MODE_MXFP8       e8m0 scales per 32 consecutive K elements of each row of A and B:
+ *                       C = bf16( sum_j acc_j * 2^(a_scale[j][m]-127) * 2^(b_scale[j][n]-127) ).
+ *                       ROCm/mori PR 785 cost table ("mxfp8") and Scope.
+ *   SG_MODE_BF16        plain GEMM: C = bf16(acc).  deepseek-ai/DeepGEMM PR 453, Summary and
+ *                       Reproduction (BF16 GEMM, fp32 accumulation).
+ *
+ * Element types: fp8 is e4m3fn (OCP OFP8: bias 7, no infinities, max 448), bf16 is
+ * the upper half of an IEEE binary32, e8m0 is an unsigned biased exponent (bias 127,
+ * 255 = NaN).  Rounding to bf16 is round-to-nearest-even.
+ *
+ * Memory layout (every pointer is a DEVICE pointer, owned by the caller, never
+ * retained by the library after the launch returns, 16-byte aligned):
+ *   A        [M][K] row-major (K contiguous): e4m3 bytes, or bf16 in SG_MODE_BF16
+ *   B        [N][K] row-major (K contiguous): same element type as A
+ *   C        [M][N] row-major bf16 (N contiguous); must not overlap A, B or the scales
+ *   ptpc        a_scale float[M],            b_scale float[N]
+ *   blockscale  a_scale float[K/128][M],     b_scale float[ceil(N/128)][K/128]
+ *   mxfp8       a_scale uint8[K/32][M],      b_scale uint8[K/32][N]     (e8m0 codes)
+ *   bf16        a_scale = b_scale = NULL
+ *
+ * Shape rules (checked on the host before anything is launched):
+ *   0 <= M <= M_max (M == 0 or N == 0 launches nothing), N % 16 == 0,
+ *   K % 16 == 0 (ptpc), K % 8 == 0 (bf16), K % 128 == 0 (blockscale),
+ *   K % 32 == 0 and M % 16 == 0 (mxfp8: the K-block-major scale rows are
+ *   fetched by TMA, whose row pitch must be a multiple of 16 bytes),
+ *   M, N, K < 2^31.  K == 0 writes C = 0.
+ *
+ * Errors: every call returns an sg_status_t and never aborts or prints (set the
+ * environment variable SG_DEBUG=1 to log rejected calls to stderr).  Kernel faults,
+ * like any CUDA asynchronous error, surface at the caller's next synchronisation.
+ *
+ * Streams: scaled_gemm_launch is asynchronous on `stream` and never synchronises.
+ * A handle is immutable after creation, so launches on one handle from several host
+ * threads or streams are safe; destroying a handle must not race a launch on it.
+ */
+#ifndef SCALED_GEMM_H
+#define SCALED_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle; the same type as cudaStream_t.  NULL = the legacy default stream. */
+typedef struct CUstream_st* sg_stream_t;
+
+/* Opaque GEMM plan, owned by the library. */
+typedef struct sg_gemm* sg_handle_t;
+
+typedef enum {
+    SG_MODE_BF16 = 0,
+    SG_MODE_PTPC = 1,
+    SG_MODE_BLOCKSCALE = 2,
+    SG_MODE_MXFP8 = 3
+} sg_mode_t;
+
+typedef enum {
+    SG_OK = 0,
+    SG_ERR_INVALID_ARG = 1,        /* NULL handle/pointer, bad mode, M > M_max, negative size */
+    SG_ERR_UNSUPPORTED_SHAPE = 2,  /* N, K or M break the shape rules above */
+    SG_ERR_MISALIGNED = 3,         /* a pointer is not 16-byte aligned */
+    SG_ERR_UNSUPPORTED_DEVICE = 4, /* the device is not compute capability 10.3 (sm_103a) */
+    SG_ERR_CUDA = 5,               /* a CUDA runtime / driver call failed */
+    SG_ERR_TIMEOUT = 6             /* a kernel wait ran past its time limit (see debug_status) */
+} sg_status_t;
+
+/* Create a plan for one (mode, N, K) that serves any M <= M_max on `device`
+ * (-1 = the current device).  The plan holds a 16-byte device status word, set
+ * up here, that kernels write only when a wait times out.
+ * On success *out receives the handle; on failure *out is set to NULL.
+ * Cited: ROCm/mori PR 809, "Using it" (one instance serves one (n, k) and any M
+ * up to m_max; bad configuration is refused at construction).                   */
+sg_status_t scaled_gemm_create(sg_handle_t* out, int mode, int64_t N, int64_t K, int64_t M_max,
+                               int device);
+
+/* Launch C = op(A, B, a_scale, b_scale) for M rows on `stream` (see the layout and
+ * shape rules above).  The call validates its arguments, builds the TMA
+ * descriptors on the host and enqueues one persistent kernel; it never blocks.
+ * Cited: ROCm/mori PR 809, "Using it" (op(a_fp8, b, a_scale, b_scale, out=));
+ * ROCm/aiter PR 6539, Test Plan (run_torch(xq, wq, x_scale, w_scale)).          */
+sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, const void* a_scale,
+                               const void* b_scale, void* C, int64_t M, sg_stream_t stream);
+
+/* Release the plan.  NULL is accepted.  Must not race a launch on the same handle. */
+sg_status_t scaled_gemm_destroy(sg_handle_t h);
+
+/* A static English description of a status code. */
+const char* scaled_gemm_status_string(sg_status_t s);
+
+/* Tile geometry the plan launches with: BM x BN output tiles, BK elements of K per
+ * pipeline stage, `stages` shared-memory stages, `grid` persistent CTAs for M = M_max.
+ * Any output pointer may be NULL.                                                */
+sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int* stages, int* grid);
+
+/* Read and clear the plan's device status word: synchronises `stream`, then stores
+ * SG_OK or SG_ERR_TIMEOUT in *code and, for a timeout, the role / wait site that gave
+ * up in *where (0 otherwise).  Every mbarrier wait in the kernels is bounded; on
+ * expiry the kernel records the site here, drains its own copies in flight, frees
+ * its tensor memory and returns, so the context stays usable.                    */
+sg_status_t scaled_gemm_debug_status(sg_handle_t h, sg_stream_t stream, int32_t* code,
+                                     int32_t* where);
+
+/* Set the time limit of every kernel-side wait for this plan (nanoseconds; 0 = the
+ * default, 4 s) and, for tests of the watchdog only, make the producer of every CTA
+ * skip its `skip_kstep`-th pipeline stage (-1 = never) so that the consumer's wait
+ * expires.  Not for production use.                                              */
+sg_status_t scaled_gemm_set_debug(sg_handle_t h, int64_t timeout_ns, int64_t skip_kstep);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SCALED_GEMM_H */
