@@ -1,7 +1,293 @@
-// sg_blockscale.cu -- placeholder until the promotion kernel lands.
+// sg_blockscale.cu -- persistent GEMM with fp32 block scales (blockscale mode).
+//
+//   C[m,n] = bf16( sum_j P_j[m,n] * sa[j][m] * sb[n/128][j] ),
+//   P_j = sum over K block j (128 wide) of e4m3(A) * e4m3(B)
+//
+// with one fp32 scale per 1 x 128 block of A (K-block major, ROCm/mori PR 809,
+// "Not done yet") and per 128 x 128 block of B (ROCm/mori PR 785, cost table:
+// the "blockscale" mode).  The tensor core's block-scaled MMA accepts only
+// power-of-two (e8m0) or e4m3 scale factors, so arbitrary fp32 scales cannot be
+// fed to it.  Instead every K block's product P_j goes into its own TMEM
+// buffer, and "promotion" warps read it with tcgen05.ld, multiply by the two
+// scales and add it to an fp32 accumulator held in registers.
+//
+// Per CTA (one per SM, persistent over 128 x 128 output tiles, so one B scale
+// block per tile):
+//   warp 0      TMA producer (A, B tiles into a 5-stage ring).
+//   warp 1      TMEM owner and MMA issuer: for K block j, wait full[s] and
+//               part_empty[p], 4 MMAs into partial buffer p (128 columns, 4
+//               buffers cycling across K blocks and tiles), commit empty[s] and
+//               part_full[p].
+//   warps 2-9   promotion + epilogue: 2 warps per TMEM lane quarter, 64 columns
+//               each; per K block wait part_full[p], tcgen05.ld, release the
+//               buffer (tcgen05.fence::before_thread_sync + arrive part_empty[p]),
+//               acc += P * (sa * sb); after the last block round to bf16 and
+//               store through shared memory and TMA.
+// The scales of K block j + 1 are loaded from global memory while block j is
+// being promoted.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sg_common.cuh"
 #include "sg_internal.h"
+
 namespace sg {
-cudaError_t blockscale_prepare() { return cudaSuccess; }
-sg_status_t blockscale_launch(const LaunchArgs&) { return SG_ERR_UNSUPPORTED_SHAPE; }
-void blockscale_config(TileConfig* c) { c->bm = 128; c->bn = 128; c->bk = 128; c->stages = 4; }
+
+namespace {
+
+constexpr int kBsBN = 128;
+constexpr int kBsStages = 5;
+constexpr int kBsParts = 4;
+constexpr int kBsWarps = 8;  // promotion warps
+constexpr int kBsThreads = 64 + 32 * kBsWarps;
+constexpr int kBsCols = 64;  // columns per promotion warp
+
+struct BsLayout {
+  static constexpr int kAStage = kBM * kRowBytes;
+  static constexpr int kBStage = kBsBN * kRowBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kBsStages * kAStage;
+  static constexpr int kOffC = kOffB + kBsStages * kBStage;
+  static constexpr int kOffBar = kOffC + kBsWarps * 2 * kCBoxBytes;
+  static constexpr int kNumBars = 2 * kBsStages + 2 * kBsParts + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16 + 4 * kBsStages;
+  static constexpr int kDynSmem = kBytes + 1024;
+  static_assert(kOffC % 1024 == 0, "alignment");
+};
+
+__global__ void __launch_bounds__(kBsThreads, 1)
+    blockscale_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  using L = BsLayout;
+  constexpr int kBK = 128;
+  constexpr int kKSteps = 4;
+  constexpr uint32_t kIdesc = instr_desc(0, 0, kBM, kBsBN);
+  constexpr uint32_t kTx = L::kAStage + L::kBStage;
+  constexpr uint32_t kTmemCols = 512;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA = smem_addr(smem + L::kOffA);
+  const uint32_t sB = smem_addr(smem + L::kOffB);
+  const uint32_t sC = smem_addr(smem + L::kOffC);
+  const uint32_t bar0 = smem_addr(smem + L::kOffBar);
+  auto full_bar = [&](int s) { return bar0 + 8 * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8 * (kBsStages + s); };
+  auto pfull_bar = [&](int q) { return bar0 + 8 * (2 * kBsStages + q); };
+  auto pempty_bar = [&](int q) { return bar0 + 8 * (2 * kBsStages + kBsParts + q); };
+  const uint32_t drain_bar = bar0 + 8 * (2 * kBsStages + 2 * kBsParts);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  uint32_t* last_par = misc + 4;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBsStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int q = 0; q < kBsParts; ++q) {
+      mbar_init(pfull_bar(q), 1);
+      mbar_init(pempty_bar(q), 32 * kBsWarps);
+    }
+    mbar_init(drain_bar, 1);
+    misc[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0, kstep = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const TileCoord tc = tile_coord(p, t);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (kstep != p.skip_kstep) {
+            mbar_arrive_expect_tx(full_bar(stage), kTx);
+            tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
+            tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kBsBN, full_bar(stage));
+            issued |= 1u << stage;
+            last_par[stage] = phase;
+          }
+          if (++stage == kBsStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kBsStages; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: one TMEM partial per K block ----------------
+    if (lane == 0) {
+      int stage = 0, part = 0;
+      uint32_t phase = 0, ppar = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(pempty_bar(part), ppar ^ 1, wd, kWhereMmaTmemEmpty) ||
+              !mbar_wait(full_bar(stage), phase, wd, kWhereMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + part * kBsBN;
+          const uint32_t a0 = sA + stage * L::kAStage;
+          const uint32_t b0 = sB + stage * L::kBStage;
+#pragma unroll
+          for (int k = 0; k < kKSteps; ++k)
+            mma_f8f6f4(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k), kIdesc, k != 0);
+          mma_commit(empty_bar(stage));
+          mma_commit(pfull_bar(part));
+          if (++stage == kBsStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (++part == kBsParts) {
+            part = 0;
+            ppar ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        mma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ---------------- promotion + epilogue ----------------
+    const int ew = warp - 2;           // 0..7
+    const int quarter = warp & 3;
+    const int col0 = (ew >> 2) * kBsCols;
+    const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
+    const int kblocks = p.k_blocks;
+    int part = 0;
+    uint32_t ppar = 0, box = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const TileCoord tc = tile_coord(p, t);
+      const int m_start = tc.mb * kBM + quarter * 32;
+      const int row = m_start + lane;
+      const bool row_ok = row < p.M;
+      const float* sa_col = p.a_scale + row;              // sa[j][row] at sa_col[j * M]
+      const float* sb_row = p.b_scale + static_cast<int64_t>(tc.nb) * kblocks;
+      float acc[kBsCols];
+#pragma unroll
+      for (int j = 0; j < kBsCols; ++j) acc[j] = 0.f;
+      float s_next = (row_ok ? __ldg(sa_col) : 0.f) * __ldg(sb_row);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const float s = s_next;
+        if (kb + 1 < kblocks)
+          s_next = (row_ok ? __ldg(sa_col + static_cast<int64_t>(kb + 1) * p.M) : 0.f) * __ldg(sb_row + kb + 1);
+        ok = mbar_wait(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + part * kBsBN + col0;
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(taddr, v0);
+        tmem_ld_32x32b_x32(taddr + 32, v1);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(pempty_bar(part));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = fmaf(__uint_as_float(v0[j]), s, acc[j]);
+          acc[32 + j] = fmaf(__uint_as_float(v1[j]), s, acc[32 + j]);
+        }
+        if (++part == kBsParts) {
+          part = 0;
+          ppar ^= 1;
+        }
+      }
+      if (!ok) break;
+      const int n_start = tc.nb * kBsBN + col0;
+      float f[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = acc[j];
+      store_box32(bufs, box, f, &tmC, n_start, m_start, p.N, p.M, lane);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) f[j] = acc[32 + j];
+      store_box32(bufs, box, f, &tmC, n_start + 32, m_start, p.N, p.M, lane);
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t blockscale_prepare() {
+  return cudaFuncSetAttribute(blockscale_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              BsLayout::kDynSmem);
+}
+
+sg_status_t blockscale_launch(const LaunchArgs& a) {
+  CUtensorMap tmA, tmB, tmC;
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, 128, kBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kBsBN,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols, kCBoxRows,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
+    return SG_ERR_CUDA;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(a.M);
+  p.N = static_cast<int32_t>(a.N);
+  p.K = static_cast<int32_t>(a.K);
+  p.m_blocks = static_cast<int32_t>((a.M + kBM - 1) / kBM);
+  p.n_blocks = static_cast<int32_t>((a.N + kBsBN - 1) / kBsBN);
+  p.k_blocks = static_cast<int32_t>(a.K / 128);
+  p.num_tiles = p.m_blocks * p.n_blocks;
+  p.skip_kstep = a.skip_kstep;
+  p.a_scale = static_cast<const float*>(a.a_scale);
+  p.b_scale = static_cast<const float*>(a.b_scale);
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
+  blockscale_gemm_kernel<<<grid, kBsThreads, BsLayout::kDynSmem, a.stream>>>(tmA, tmB, tmC, p);
+  return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
+}
+
+void blockscale_config(TileConfig* c) {
+  c->bm = kBM;
+  c->bn = kBsBN;
+  c->bk = 128;
+  c->stages = kBsStages;
+}
+
 }  // namespace sg

@@ -49,59 +49,76 @@ __device__ __forceinline__ uint32_t cbox_chunk_addr(uint32_t box, int row, int c
   return box + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
 }
 
+// Round 32 fp32 values of one row to bf16 and store the warp's 32 x 32 box.
+// The warp owns two kCBoxBytes store boxes at `bufs` and alternates between them
+// with the running counter `box`: the store that last read the box about to be
+// written was committed two boxes ago, so at most one newer store may still be
+// reading shared memory.  Every writer fences its generic stores into
+// the async proxy before lane 0 issues the TMA store (deepseek-ai/DeepGEMM
+// PR 453, Fix: the fence is executed by all threads, not only the issuing one).
+__device__ __forceinline__ void store_box32(uint32_t bufs, uint32_t& box, const float (&f)[32],
+                                            const CUtensorMap* tmC, int x, int y, int N, int M,
+                                            int lane) {
+  const uint32_t buf = bufs + (box & 1u) * kCBoxBytes;
+  ++box;
+  uint32_t packed[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) packed[j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st_shared_v4(cbox_chunk_addr(buf, lane, k), packed[4 * k], packed[4 * k + 1], packed[4 * k + 2],
+                 packed[4 * k + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (x < N && y < M) tma_store_2d(tmC, buf, x, y);
+    bulk_commit_group();
+  }
+}
+
 // Epilogue worker for one output tile, run by one warp on 32 rows (its TMEM lane
-// quarter) and columns [col0, col0 + ncols) of the tile.  Values are read from
-// TMEM, multiplied by `row_scale * col_scale[c]` when the mode has scales, rounded
-// to bf16 and stored through two alternating 2 KB shared-memory boxes by TMA.
-//
-//   taddr      TMEM address of (lane quarter base, accumulator column col0)
-//   bufs       two kCBoxBytes store boxes owned by this warp
-//   col_scale  per-column scales in shared memory (nullptr: no scaling)
-//   release    called once after the last TMEM load has completed
+// quarter) and NCOLS columns starting at the accumulator address `taddr`.  Values
+// are read from TMEM, multiplied by `row_scale * col_scale[c]` when SCALED,
+// rounded to bf16 and stored through the warp's two store boxes `bufs` (box
+// counter `box`).  `release()` runs once, right after the last TMEM load.
 template <int NCOLS, bool SCALED, typename Release>
-__device__ __forceinline__ void epilogue_tile(uint32_t taddr, uint32_t bufs, const float* col_scale,
+__device__ __forceinline__ void epilogue_tile(uint32_t taddr, uint32_t bufs, uint32_t& box,
+                                              const float* col_scale,
                                               float row_scale, const CUtensorMap* tmC, int n_start,
                                               int m_start, int N, int M, int lane,
                                               Release&& release) {
-  static_assert(NCOLS % 64 == 0, "epilogue works in 64-column steps");
+  static_assert(NCOLS % 32 == 0, "epilogue works in 32-column boxes");
+  auto convert = [&](const uint32_t (&v)[32], int cc, float (&f)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      f[j] = __uint_as_float(v[j]);
+      if constexpr (SCALED) f[j] = f[j] * row_scale * col_scale[cc + j];
+    }
+  };
 #pragma unroll 1
-  for (int c = 0; c < NCOLS; c += 64) {
+  for (int c = 0; c + 64 <= NCOLS; c += 64) {
     uint32_t v0[32], v1[32];
     tmem_ld_32x32b_x32(taddr + c, v0);
     tmem_ld_32x32b_x32(taddr + c + 32, v1);
     tmem_wait_ld();
     if (c + 64 == NCOLS) release();
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint32_t* v = half ? v1 : v0;
-      const int cc = c + half * 32;
-      uint32_t packed[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float f0 = __uint_as_float(v[2 * j]);
-        float f1 = __uint_as_float(v[2 * j + 1]);
-        if constexpr (SCALED) {
-          f0 = f0 * row_scale * col_scale[cc + 2 * j];
-          f1 = f1 * row_scale * col_scale[cc + 2 * j + 1];
-        }
-        packed[j] = pack_bf16x2(f0, f1);
-      }
-      const uint32_t buf = bufs + half * kCBoxBytes;
-      // The store that last read this box was committed two boxes ago.
-      if (lane == 0) bulk_wait_group_read<1>();
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        st_shared_v4(cbox_chunk_addr(buf, lane, k), packed[4 * k], packed[4 * k + 1],
-                     packed[4 * k + 2], packed[4 * k + 3]);
-      // Every writer orders its generic stores before the async-proxy read.
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        if (n_start + cc < N && m_start < M) tma_store_2d(tmC, buf, n_start + cc, m_start);
-        bulk_commit_group();
-      }
-    }
+    float f[32];
+    convert(v0, c, f);
+    store_box32(bufs, box, f, tmC, n_start + c, m_start, N, M, lane);
+    convert(v1, c + 32, f);
+    store_box32(bufs, box, f, tmC, n_start + c + 32, m_start, N, M, lane);
+  }
+  if constexpr (NCOLS % 64 == 32) {
+    constexpr int c = NCOLS - 32;
+    uint32_t v0[32];
+    tmem_ld_32x32b_x32(taddr + c, v0);
+    tmem_wait_ld();
+    release();
+    float f[32];
+    convert(v0, c, f);
+    store_box32(bufs, box, f, tmC, n_start + c, m_start, N, M, lane);
   }
 }
 

@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
     float* col_scale = reinterpret_cast<float*>(smem + L::kOffScale) + ew * kColsPerWarp;
     int it = 0;
+    uint32_t box = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
       const TileCoord tc = tile_coord(p, t);
       const int acc = it & 1;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              acc * kAccStride + col0;
-      epilogue_tile<kColsPerWarp, kScaled>(taddr, bufs, col_scale, row_scale, &tmC, n_start,
+      epilogue_tile<kColsPerWarp, kScaled>(taddr, bufs, box, col_scale, row_scale, &tmC, n_start,
                                           m_start, p.N, p.M, lane, [&]() {
                                             tc_fence_before();
                                             mbar_arrive(tempty_bar(acc));

@@ -113,3 +113,30 @@ def test_m_zero_is_a_no_op(gpu):
         assert np.all(dc.c_bits() == gpu.NAN_BF16)
     finally:
         gpu.binding.scaled_gemm_destroy(h)
+
+
+@pytest.mark.parametrize(
+    "M,N,K",
+    [
+        (16, 16, 32),       # one partial K block (1 of 4 scale blocks)
+        (128, 224, 128),    # one tile
+        (144, 240, 416),    # ragged M, N and K (K = 3.25 stages)
+        (256, 512, 1792),
+        (384, 7168, 256),   # the full weight width, two K blocks
+    ],
+)
+def test_mxfp8_shapes(gpu, M, N, K):
+    _run_full(gpu, synth.make_case("mxfp8", M, N, K, seed=M + K, b_std=0.02), launches=8)
+
+
+@pytest.mark.parametrize(
+    "M,N,K",
+    [
+        (1, 16, 128),
+        (128, 128, 256),
+        (200, 272, 640),    # ragged M and N (N block partially outside)
+        (256, 512, 2048),
+    ],
+)
+def test_blockscale_shapes(gpu, M, N, K):
+    _run_full(gpu, synth.make_case("blockscale", M, N, K, seed=M + K, b_std=0.02), launches=8)
