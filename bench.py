@@ -1,0 +1,493 @@
+"""Benchmark of the scaled FP8 / BF16 GEMM hot path on GB300.
+
+One step = one launch of every workload in the suite below, each on its own
+synthetic inputs already resident in HBM: the M x 7168 x K ptpc shapes (tail-only
+K=256, K=512, K=1792), blockscale 16384x7168x2048, mxfp8 32768x7168x1792, the
+unpadded-N ptpc shapes at K=7168 (N = 6288, 3648, 6400) and the BF16
+[4096,1024]x[1024,896] GEMM.  `value` is the suite's total FLOPs (2MNK per GEMM)
+divided by its device time, in TFLOP/s; per-workload times, TFLOP/s and
+fractions of peak are in `per_config`.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same suite on its own GPU (replicas:
+the GEMM needs no exchange); the step time is the max over ranks and `value`
+counts the work of all ranks.  `--impl reference` times the CPU oracle on a
+bounded row sample of the same workloads instead (rank 0 only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "scaled-FP8 GEMM TFLOPS & % FP8 peak at M×7168×K; bad launches per 20 (must be 0)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Control:
+    """Host-side control plane across replicas (gloo): barrier and reductions."""
+
+    def __init__(self, world):
+        self.world = world
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def max(self, x):
+        if not self.dist:
+            return float(x)
+        t = torch.tensor([float(x)], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x):
+        if not self.dist:
+            return float(x)
+        t = torch.tensor([float(x)], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+
+
+def aggregate(control, local_flops, local_seconds):
+    """Whole-job throughput: work of all ranks over the slowest rank's time."""
+    total = control.sum(local_flops)
+    t = control.max(local_seconds)
+    return total, t, (total / t / 1e12 if t > 0 else 0.0)
+
+
+def make_suite():
+    cases, cache = [], {}
+    for name in synth.SUITE:
+        mode, M, N, K, seed, a_std, b_std = synth.CONFIGS[name]
+        cases.append((name, synth.make_case(mode, M, N, K, seed=seed, a_std=a_std, b_std=b_std, cache=cache)))
+    return cases
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while a region runs."""
+
+    QUERY = (
+        "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+        "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+    )
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL,
+            )
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[4], f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r[2] > 300.0] or rows  # samples under load (power)
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for nm, v in zip(names, r[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {
+            "sm_mhz": statistics.median(r[0] for r in loaded),
+            "sm_max_mhz": max(r[1] for r in rows),
+            "power_w_max": max(r[2] for r in rows),
+            "reasons": sorted(reasons),
+            "samples": len(rows),
+            "samples_under_load": len(loaded),
+        }
+
+
+# --------------------------------------------------------------------------- oracle baseline
+
+
+def cpu_baseline(cases, rows, seconds_cap=None):
+    """The CPU oracle on rows [0, rows) of every workload: (TFLOP/s, seconds, threads, flops)."""
+    import oracle
+
+    flops = 0.0
+    t0 = time.perf_counter()
+    for name, c in cases:
+        r = min(rows, c.M)
+        oracle.gemm(c.mode, *c.numpy(), rows=(0, r), want_r=False)
+        flops += 2.0 * r * c.N * c.K
+        if seconds_cap and time.perf_counter() - t0 > seconds_cap:
+            break
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, oracle.num_threads(), flops
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args, control, rank, local):
+    from fp8_scaled_gemm_sm_gb300 import binding, build
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_kind = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    fp8_peak_burst = 2.0 * peaks["bf16_tflops"]
+    bf16_peak = peaks["bf16_tflops_sustained"]
+    hbm = peaks["hbm_gbs"]
+
+    cases = make_suite()
+    stream = torch.cuda.Stream(dev)
+    sraw = stream.cuda_stream
+    work = []
+    for name, c in cases:
+        d = {
+            "name": name,
+            "case": c,
+            "A": c.A.to(dev),
+            "B": c.B.to(dev),
+            "sa": None if c.sa is None else c.sa.to(dev),
+            "sb": None if c.sb is None else c.sb.to(dev),
+            "C": torch.empty((c.M, c.N), dtype=torch.bfloat16, device=dev),
+            "h": binding.scaled_gemm_create(c.mode, c.N, c.K, c.M, local),
+        }
+        d["cfg"] = binding.scaled_gemm_get_config(d["h"])
+        work.append(d)
+    torch.cuda.synchronize()
+
+    def launch(d, C=None):
+        binding.scaled_gemm_launch(
+            d["h"], d["A"].data_ptr(), d["B"].data_ptr(),
+            0 if d["sa"] is None else d["sa"].data_ptr(),
+            0 if d["sb"] is None else d["sb"].data_ptr(),
+            (d["C"] if C is None else C).data_ptr(), d["case"].M, sraw,
+        )
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for d in work:
+                launch(d)
+    torch.cuda.synchronize()
+
+    # timed steps: one event pair around the step plus one per GEMM
+    n = len(work)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)] for _ in range(args.steps)]
+    e_all0, e_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    control.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e_all0.record(stream)
+        for s in range(args.steps):
+            for i, d in enumerate(work):
+                ev[s][i][0].record(stream)
+                launch(d)
+                ev[s][i][1].record(stream)
+        e_all1.record(stream)
+    torch.cuda.synchronize()
+    control.barrier()
+    wall1 = time.perf_counter()
+    clk = clocks.stop()
+    local_s = e_all0.elapsed_time(e_all1) / 1e3
+    flops_step = sum(d["case"].flops for d in work)
+    total_flops, t_max, value = aggregate(control, flops_step * args.steps, local_s)
+
+    per = {}
+    for i, d in enumerate(work):
+        c = d["case"]
+        ms = [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps)]
+        us = 1e3 * sum(ms) / len(ms)
+        tf = c.flops / (us * 1e-6) / 1e12
+        byts = synth.gemm_bytes(c.mode, c.M, c.N, c.K)
+        peak = bf16_peak if c.mode == "bf16" else fp8_peak
+        per[d["name"]] = {
+            "mode": c.mode, "M": c.M, "N": c.N, "K": c.K,
+            "us": round(us, 2), "us_min": round(1e3 * min(ms), 2),
+            "tflops": round(tf, 1),
+            "frac_peak": round(tf / peak, 3),
+            "frac_peak_burst": round(tf / (peaks["bf16_tflops"] if c.mode == "bf16" else fp8_peak_burst), 3),
+            "gbs": round(byts / (us * 1e-6) / 1e9, 1),
+            "frac_hbm": round(byts / (us * 1e-6) / 1e9 / hbm, 3),
+            "tile": "%dx%d" % (d["cfg"]["bm"], d["cfg"]["bn"]), "grid": d["cfg"]["grid"],
+        }
+
+    # dominant kernel: the workload with the largest device time in the step
+    dom = max(per, key=lambda k: per[k]["us"])
+    pc = per[dom]
+    dom_flops = 2.0 * pc["M"] * pc["N"] * pc["K"]
+    achieved = dom_flops / (pc["us"] * 1e-6) / 1e12
+    dom_peak = bf16_peak if pc["mode"] == "bf16" else fp8_peak
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            if tj.get("workload") == dom and tj.get("kernel_rev") == kernel_revision():
+                traffic = tj.get("bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    roofline = {
+        "bound": "tensor", "achieved": round(achieved, 1), "peak": round(dom_peak, 1), "unit": "TFLOP/s",
+        "frac": round(achieved / dom_peak, 3), "traffic": traffic,
+        "kernel": ("dense_gemm_kernel<ptpc>" if pc["mode"] == "ptpc" else pc["mode"] + "_gemm_kernel"),
+        "workload": dom,
+        "peak_source": "%s: 2 x bf16_tflops_sustained (fp8 = 2 x bf16 nominal ratio)" % peak_kind,
+    }
+
+    # bad launches: 20 launches per workload into NaN-poisoned outputs, each
+    # bit-identical to the first and NaN-free (parity against the oracle is in tests/)
+    bad = 0
+    with torch.cuda.stream(stream):
+        for d in work:
+            first = None
+            for _ in range(20):
+                d["C"].view(torch.int16).fill_(0x7FC0)
+                launch(d)
+                cur = d["C"].view(torch.int16)
+                isnan = torch.isnan(d["C"]).any()
+                if first is None:
+                    first = cur.clone()
+                    ok = not bool(isnan)
+                else:
+                    ok = (not bool(isnan)) and torch.equal(cur, first)
+                bad += 0 if ok else 1
+            del first
+    torch.cuda.synchronize()
+    status_bad = 0
+    for d in work:
+        code, _ = binding.scaled_gemm_debug_status(d["h"], sraw)
+        status_bad += code != 0
+
+    # end to end through the C ABI with host buffers: H2D inputs, GEMM, D2H C
+    e2e = run_e2e(work, launch, stream, args, control, dev)
+
+    cpu = None
+    if rank == 0 and control.world == 1 and not args.no_cpu_baseline:
+        v, dt, cores, fl = cpu_baseline(cases, args.cpu_rows)
+        cpu = {
+            "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "rows [0,%d) of every suite workload (%.1f GFLOP, %.1f s)" % (args.cpu_rows, fl / 1e9, dt),
+        }
+
+    for d in work:
+        binding.scaled_gemm_destroy(d["h"])
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": control.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 (bf16 x bf16 for the BF16 GEMM), fp32 accumulate, bf16 out",
+        "data": "synthetic (seeded normals quantised per the workload's scale mode)",
+        "config": {
+            "workload": "suite: " + ", ".join(synth.SUITE),
+            "parallelism": "replicas" if control.world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (suite operands %.2f GB; each GEMM's operands last touched one full step earlier)"
+            % (sum(d["A"].numel() * d["A"].element_size() + d["B"].numel() * d["B"].element_size() for d in work) / 1e9),
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": args.steps * n,
+        "bad_launches": {"per_workload": 20, "workloads": n, "bad": bad, "watchdog_timeouts": status_bad},
+        "per_config": per,
+        "wall_s_timed": round(wall1 - wall0, 4),
+        "peaks": {"source": peak_kind, "fp8_tflops_sustained": fp8_peak, "fp8_tflops_burst": fp8_peak_burst,
+                  "bf16_tflops_sustained": bf16_peak, "hbm_gbs": hbm},
+    }
+    return line
+
+
+def run_e2e(work, launch, stream, args, control, dev):
+    steps = max(1, args.e2e_steps)
+    host_in, host_out, dev_in = [], [], []
+    h2d = d2h = 0
+    for d in work:
+        ins = []
+        for key in ("A", "B", "sa", "sb"):
+            t = d[key]
+            if t is None:
+                ins.append(None)
+                continue
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            ins.append(h)
+            h2d += t.numel() * t.element_size()
+        host_in.append(ins)
+        host_out.append(torch.empty(d["C"].shape, dtype=d["C"].dtype, pin_memory=True))
+        d2h += d["C"].numel() * d["C"].element_size()
+    torch.cuda.synchronize()
+
+    def step():
+        for d, ins, out in zip(work, host_in, host_out):
+            for key, h in zip(("A", "B", "sa", "sb"), ins):
+                if h is not None:
+                    d[key].copy_(h, non_blocking=True)
+            launch(d)
+            out.copy_(d["C"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    control.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    control.barrier()
+    secs = e0.elapsed_time(e1) / 1e3
+    flops = steps * sum(d["case"].flops for d in work)
+    _, _, v = aggregate(control, flops, secs)
+    return {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": round(1e3 * secs / steps, 3)}
+
+
+def kernel_revision():
+    """Hash of the CUDA sources, to tell whether stored counters still apply."""
+    import hashlib
+
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "fp8_scaled_gemm_sm_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+# --------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args, control, rank):
+    if rank != 0:
+        return None
+    cases = make_suite()
+    rows = args.ref_rows
+    times, flops = [], 0.0
+    for s in range(args.warmup + args.steps):
+        v, dt, cores, fl = cpu_baseline(cases, rows)
+        if s >= args.warmup:
+            times.append(dt)
+            flops = fl
+    t = sum(times)
+    value = flops * len(times) / t / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": control.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (CPU oracle: exact e4m3/e8m0 decode, binary64 accumulation)",
+        "data": "synthetic (seeded normals quantised per the workload's scale mode)",
+        "config": {"workload": "suite: " + ", ".join(synth.SUITE), "sample": "rows [0,%d) of every workload per step" % rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "rows [0,%d) of every suite workload per step" % rows},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3  # timing rule: at least 3 warm-up steps
+    world, rank, local = dist_env()
+    control = Control(world)
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, control, rank)
+        else:
+            line = run_gpu(args, control, rank, local)
+    finally:
+        control.close()
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -113,26 +113,50 @@ def _draw(gen, rows, cols, std):
     return torch.randn(rows, cols, generator=gen, dtype=torch.float32) * std
 
 
-def make_case(mode: str, M: int, N: int, K: int, seed: int = 0, a_std: float = 1.0, b_std: float = 1.0) -> Case:
-    """Seeded synthetic case in the given scale mode (A drawn first, then B)."""
-    g = torch.Generator("cpu")
-    g.manual_seed(seed)
-    a = _draw(g, M, K, a_std)
+_QUANT_A = {
+    "ptpc": quantize_e4m3_rows,
+    "blockscale": quantize_e4m3_blocks_1x128,
+    "mxfp8": quantize_mx_rows,
+}
+_QUANT_B = {
+    "ptpc": quantize_e4m3_rows,
+    "blockscale": quantize_e4m3_blocks_128x128,
+    "mxfp8": quantize_mx_rows,
+}
+
+
+def make_case(mode: str, M: int, N: int, K: int, seed: int = 0, a_std: float = 1.0, b_std: float = 1.0,
+              cache: Optional[dict] = None) -> Case:
+    """Seeded synthetic case in the given scale mode (A drawn first, then B).
+
+    ``cache`` (optional dict) reuses the quantised A and the generator state
+    after A between cases that share (mode, M, K, seed, a_std): the values are
+    exactly those of a fresh draw.
+    """
+    if mode not in ("bf16",) and mode not in _QUANT_A:
+        raise ValueError("unknown mode %r" % mode)
+    key = (mode, M, K, seed, a_std)
+    if cache is not None and key in cache:
+        qa, sa, state = cache[key]
+        g = torch.Generator("cpu")
+        g.set_state(state)
+    else:
+        g = torch.Generator("cpu")
+        g.manual_seed(seed)
+        a = _draw(g, M, K, a_std)
+        if mode == "bf16":
+            qa, sa = a.bfloat16().contiguous(), None
+        else:
+            qa, sa = _QUANT_A[mode](a)
+            qa = qa.contiguous()
+        del a
+        if cache is not None:
+            cache[key] = (qa, sa, g.get_state())
     b = _draw(g, N, K, b_std)
     if mode == "bf16":
-        return Case(mode, M, N, K, a.bfloat16().contiguous(), b.bfloat16().contiguous(), None, None, seed)
-    if mode == "ptpc":
-        qa, sa = quantize_e4m3_rows(a)
-        qb, sb = quantize_e4m3_rows(b)
-    elif mode == "blockscale":
-        qa, sa = quantize_e4m3_blocks_1x128(a)
-        qb, sb = quantize_e4m3_blocks_128x128(b)
-    elif mode == "mxfp8":
-        qa, sa = quantize_mx_rows(a)
-        qb, sb = quantize_mx_rows(b)
-    else:
-        raise ValueError("unknown mode %r" % mode)
-    return Case(mode, M, N, K, qa.contiguous(), qb.contiguous(), sa, sb, seed)
+        return Case(mode, M, N, K, qa, b.bfloat16().contiguous(), None, None, seed)
+    qb, sb = _QUANT_B[mode](b)
+    return Case(mode, M, N, K, qa, qb.contiguous(), sa, sb, seed)
 
 
 def make_int_case(M: int, N: int, K: int, lo: int = -16, hi: int = 16, seed: int = 0) -> Case:
