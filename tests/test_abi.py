@@ -1,0 +1,78 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/*.h declares, and rejects bad arguments on the host before touching
+CUDA (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp8_scaled_gemm_sm_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(scaled_gemm_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    for n in ("scaled_gemm_create", "scaled_gemm_launch", "scaled_gemm_destroy", "scaled_gemm_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(binding.LIB_PATH)
+    for n in _declared():
+        assert hasattr(raw, n), n
+        assert n in binding.SIGNATURES, "binding lacks " + n
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert binding.scaled_gemm_status_string(code)
+    assert "unknown" in binding.scaled_gemm_status_string(99)
+
+
+@pytest.mark.parametrize(
+    "mode,N,K,M_max,status",
+    [
+        (7, 256, 256, 16, 1),        # bad mode
+        ("ptpc", -16, 256, 16, 1),   # negative size
+        ("ptpc", 100, 256, 16, 2),   # N % 16
+        ("ptpc", 256, 24, 16, 2),    # K % 16
+        ("bf16", 256, 12, 16, 2),    # K % 8
+        ("blockscale", 256, 192, 16, 2),  # K % 128
+        ("mxfp8", 256, 48, 16, 2),   # K % 32
+        ("ptpc", 1 << 31, 256, 16, 2),  # too large
+    ],
+)
+def test_create_rejects_bad_shapes_on_the_host(lib, mode, N, K, M_max, status):
+    with pytest.raises(binding.ScaledGemmError) as e:
+        binding.scaled_gemm_create(mode, N, K, M_max)
+    assert e.value.status == status
+
+
+def test_null_handle_is_rejected(lib):
+    L = binding.lib()
+    assert L.scaled_gemm_launch(None, None, None, None, None, None, 16, None) == 1
+    assert L.scaled_gemm_destroy(None) == 0
+    assert L.scaled_gemm_get_config(None, None, None, None, None, None) == 1
+    assert L.scaled_gemm_set_debug(None, 0, -1) == 1
+    code = ctypes.c_int32()
+    assert L.scaled_gemm_debug_status(None, None, ctypes.byref(code), None) == 1
+    assert L.scaled_gemm_create(None, 1, 256, 256, 16, -1) == 1
