@@ -34,6 +34,7 @@ SIGNATURES = {
     "scaled_gemm_get_config": (_int, [_vp] + [ctypes.POINTER(_int)] * 5),
     "scaled_gemm_debug_status": (_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "scaled_gemm_set_debug": (_int, [_vp, _i64, _i64]),
+    "scaled_gemm_launch_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
 }
 
 
@@ -84,6 +85,14 @@ def scaled_gemm_launch(h, A, B, a_scale, b_scale, C, M, stream=0):
     _check(
         lib().scaled_gemm_launch(h, A, B, a_scale or None, b_scale or None, C, int(M), stream or None),
         "scaled_gemm_launch",
+    )
+
+
+def scaled_gemm_launch_noalloc(A, B, a_scale, b_scale, C, M, N, K, stream=0):
+    """ptpc launch without a handle and without any device allocation (see the C header)."""
+    _check(
+        lib().scaled_gemm_launch_noalloc(A, B, a_scale, b_scale, C, int(M), int(N), int(K), stream or None),
+        "scaled_gemm_launch_noalloc",
     )
 
 

@@ -26,6 +26,10 @@ struct LaunchArgs {
   int32_t skip_kstep;   // watchdog tests: -1 = off
 };
 
+// Mode numbers as the launchers take them (equal to sg_mode_t).
+constexpr int kModeBf16Host = SG_MODE_BF16;
+constexpr int kModePtpcHost = SG_MODE_PTPC;
+
 struct TileConfig {
   int bm, bn, bk, stages;
 };

@@ -125,6 +125,33 @@ sg_status_t scaled_gemm_debug_status(sg_handle_t h, sg_stream_t stream, int32_t*
  * expires.  Not for production use.                                              */
 sg_status_t scaled_gemm_set_debug(sg_handle_t h, int64_t timeout_ns, int64_t skip_kstep);
 
+/* ptpc GEMM for callers that cannot allocate device memory.  (The paper has no
+ * counterpart: this entry point belongs to this library's interface only.)
+ *
+ * scaled_gemm_create allocates the kernel's 16-byte watchdog status record with
+ * cudaMalloc, which some callers cannot do: code running inside a custom
+ * allocator or a memory-pool callback (where a nested cudaMalloc would re-enter
+ * the allocator), or processes whose device memory is all reserved up front by a
+ * pool that owns every allocation.  This call needs no handle and allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine): the status record lives in a
+ * 64-byte static device array inside the library, which every GPU that loads
+ * the library holds until the process exits.  A launch that would need more
+ * scratch than that array holds is rejected with SG_ERR_UNSUPPORTED_SHAPE.
+ *
+ * Operands, layouts and shape rules are those of SG_MODE_PTPC above, with M, N, K
+ * given directly (K == 0 is rejected; use scaled_gemm_launch).  The current
+ * device is used.  The first call on a device sets it up (checks compute
+ * capability 10.3, looks up the array's device address, sets the kernel's
+ * shared-memory limit); make that first call before any stream capture.  Every
+ * call clears the shared status record on `stream` before its kernel and the
+ * record keeps the last call's contents; calls whose kernels overlap on the GPU
+ * race on it, so serialise them (one stream) if the record matters.  The record
+ * cannot be read through this entry point; use the handle API to diagnose a
+ * watchdog timeout.                                                              */
+sg_status_t scaled_gemm_launch_noalloc(const void* A, const void* B, const void* a_scale,
+                                       const void* b_scale, void* C, int64_t M, int64_t N,
+                                       int64_t K, sg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,3 +76,14 @@ def test_null_handle_is_rejected(lib):
     code = ctypes.c_int32()
     assert L.scaled_gemm_debug_status(None, None, ctypes.byref(code), None) == 1
     assert L.scaled_gemm_create(None, 1, 256, 256, 16, -1) == 1
+
+
+def test_noalloc_rejects_bad_arguments_on_the_host(lib):
+    L = binding.lib()
+    f = L.scaled_gemm_launch_noalloc
+    assert f(None, None, None, None, None, 16, 100, 256, None) == 2   # N % 16
+    assert f(None, None, None, None, None, 16, 256, 24, None) == 2    # K % 16
+    assert f(None, None, None, None, None, -1, 256, 256, None) == 1   # negative
+    assert f(None, None, None, None, None, 0, 256, 256, None) == 0    # empty: nothing to do
+    assert f(None, None, None, None, None, 16, 256, 256, None) == 1   # NULL operands
+    assert f(16, 32, 48, 64, 8, 16, 256, 256, None) == 3              # C misaligned
