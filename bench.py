@@ -98,10 +98,13 @@ def aggregate(control, local_flops, local_seconds):
     return total, t, (total / t / 1e12 if t > 0 else 0.0)
 
 
-def make_suite():
+def make_suite(only=None, rows=None):
+    """The suite's cases; `only` keeps one workload and `rows` shrinks its M (profiling runs)."""
     cases, cache = [], {}
-    for name in synth.SUITE:
+    for name in synth.SUITE if only is None else [only]:
         mode, M, N, K, seed, a_std, b_std = synth.CONFIGS[name]
+        if rows:
+            M = rows
         cases.append((name, synth.make_case(mode, M, N, K, seed=seed, a_std=a_std, b_std=b_std, cache=cache)))
     return cases
 
@@ -209,7 +212,7 @@ def run_gpu(args, control, rank, local):
     bf16_peak = peaks["bf16_tflops_sustained"]
     hbm = peaks["hbm_gbs"]
 
-    cases = make_suite()
+    cases = make_suite(args.only, args.rows)
     stream = torch.cuda.Stream(dev)
     sraw = stream.cuda_stream
     work = []
@@ -293,15 +296,7 @@ def run_gpu(args, control, rank, local):
     dom_flops = 2.0 * pc["M"] * pc["N"] * pc["K"]
     achieved = dom_flops / (pc["us"] * 1e-6) / 1e12
     dom_peak = bf16_peak if pc["mode"] == "bf16" else fp8_peak
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            tj = json.load(open(tpath))
-            if tj.get("workload") == dom and tj.get("kernel_rev") == kernel_revision():
-                traffic = tj.get("bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
+    traffic = stored_traffic(dom)
     roofline = {
         "bound": "tensor", "achieved": round(achieved, 1), "peak": round(dom_peak, 1), "unit": "TFLOP/s",
         "frac": round(achieved / dom_peak, 3), "traffic": traffic,
@@ -314,7 +309,7 @@ def run_gpu(args, control, rank, local):
     # bit-identical to the first and NaN-free (parity against the oracle is in tests/)
     bad = 0
     with torch.cuda.stream(stream):
-        for d in work:
+        for d in ([] if args.no_bad_check else work):
             first = None
             for _ in range(20):
                 d["C"].view(torch.int16).fill_(0x7FC0)
@@ -335,7 +330,7 @@ def run_gpu(args, control, rank, local):
         status_bad += code != 0
 
     # end to end through the C ABI with host buffers: H2D inputs, GEMM, D2H C
-    e2e = run_e2e(work, launch, stream, args, control, dev)
+    e2e = None if args.no_e2e else run_e2e(work, launch, stream, args, control, dev)
 
     cpu = None
     if rank == 0 and control.world == 1 and not args.no_cpu_baseline:
@@ -355,7 +350,7 @@ def run_gpu(args, control, rank, local):
         "dtype": "e4m3 x e4m3 (bf16 x bf16 for the BF16 GEMM), fp32 accumulate, bf16 out",
         "data": "synthetic (seeded normals quantised per the workload's scale mode)",
         "config": {
-            "workload": "suite: " + ", ".join(synth.SUITE),
+            "workload": "suite: " + ", ".join(name for name, _ in cases) + (" (M=%d)" % args.rows if args.rows else ""),
             "parallelism": "replicas" if control.world > 1 else "single GPU",
             "l2": "inputs larger than L2 (suite operands %.2f GB; each GEMM's operands last touched one full step earlier)"
             % (sum(d["A"].numel() * d["A"].element_size() + d["B"].numel() * d["B"].element_size() for d in work) / 1e9),
@@ -365,7 +360,8 @@ def run_gpu(args, control, rank, local):
         "e2e": e2e,
         "clocks": clk,
         "gpu_launches": args.steps * n,
-        "bad_launches": {"per_workload": 20, "workloads": n, "bad": bad, "watchdog_timeouts": status_bad},
+        "bad_launches": {"per_workload": 0 if args.no_bad_check else 20, "workloads": n, "bad": bad,
+                         "watchdog_timeouts": status_bad},
         "per_config": per,
         "wall_s_timed": round(wall1 - wall0, 4),
         "peaks": {"source": peak_kind, "fp8_tflops_sustained": fp8_peak, "fp8_tflops_burst": fp8_peak_burst,
@@ -422,6 +418,20 @@ def run_e2e(work, launch, stream, args, control, dev):
             "steps": steps, "ms_per_step": round(1e3 * secs / steps, 3)}
 
 
+def stored_traffic(workload):
+    """DRAM bytes per launch of `workload` from profiles/traffic.txt, if they were
+    measured on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    rev = kernel_revision()
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == workload and f[1] == rev:
+            return float(f[2])
+    return None
+
+
 def kernel_revision():
     """Hash of the CUDA sources, to tell whether stored counters still apply."""
     import hashlib
@@ -473,6 +483,10 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--no-bad-check", action="store_true", help="skip the 20-launch check (profiling runs)")
+    ap.add_argument("--only", default=None, choices=synth.SUITE, help="one workload (profiling runs)")
+    ap.add_argument("--rows", type=int, default=None, help="override M of the workload(s) (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3  # timing rule: at least 3 warm-up steps
