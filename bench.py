@@ -424,7 +424,7 @@ def stored_traffic(workload):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    rev = kernel_revision()
+    rev = kernel_revision(synth.CONFIGS[workload][0])
     for line in open(path):
         f = line.split()
         if len(f) >= 3 and not line.startswith("#") and f[0] == workload and f[1] == rev:
@@ -432,15 +432,23 @@ def stored_traffic(workload):
     return None
 
 
-def kernel_revision():
-    """Hash of the CUDA sources, to tell whether stored counters still apply."""
+KERNEL_FILES = {
+    "ptpc": ["sg_dense.cu", "sg_common.cuh", "sg_ptx.cuh"],
+    "bf16": ["sg_dense.cu", "sg_common.cuh", "sg_ptx.cuh"],
+    "mxfp8": ["sg_mxfp8.cu", "sg_common.cuh", "sg_ptx.cuh"],
+    "blockscale": ["sg_blockscale.cu", "sg_common.cuh", "sg_ptx.cuh"],
+}
+
+
+def kernel_revision(mode="ptpc"):
+    """Hash of the CUDA sources of one kernel family, to tell whether stored
+    counters still apply to the code that runs."""
     import hashlib
 
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "fp8_scaled_gemm_sm_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_FILES[mode]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:12]
 
 
