@@ -184,7 +184,7 @@ sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int
   sg::TileConfig c{};
   switch (h->mode) {
     case SG_MODE_BF16:
-    case SG_MODE_PTPC: sg::dense_config(h->mode, &c); break;
+    case SG_MODE_PTPC: sg::dense_config(h->mode, h->K, &c); break;
     case SG_MODE_MXFP8: sg::mxfp8_config(&c); break;
     case SG_MODE_BLOCKSCALE: sg::blockscale_config(&c); break;
   }

@@ -23,8 +23,7 @@
 //               buffer (tcgen05.fence::before_thread_sync + arrive part_empty[p]),
 //               acc += P * (sa * sb); after the last block round to bf16 and
 //               store through shared memory and TMA.
-// The scales of K block j + 1 are loaded from global memory while block j is
-// being promoted.
+// The scales are loaded from global memory four K blocks ahead of their use.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -188,45 +187,70 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     int part = 0;
     uint32_t ppar = 0, box = 0;
     bool ok = true;
+    // Scale products s = sa[j][row] * sb[nb][j] are loaded kScaleAhead K blocks
+    // before they are needed (a ring of registers), and the first ones of the next
+    // tile are loaded before this tile's epilogue, so no promotion step waits on
+    // a global load.
+    constexpr int kScaleAhead = 4;
+    float ring_a[kScaleAhead], ring_b[kScaleAhead];
+    auto load_scales = [&](int t, int kb, float& sa_out, float& sb_out) {
+      const TileCoord c = tile_coord(p, t);
+      const int row = c.mb * kBM + quarter * 32 + lane;
+      sa_out = row < p.M ? __ldg(p.a_scale + static_cast<int64_t>(kb) * p.M + row) : 0.f;
+      sb_out = __ldg(p.b_scale + static_cast<int64_t>(c.nb) * kblocks + kb);
+    };
+    if (static_cast<int>(blockIdx.x) < p.num_tiles) {
+#pragma unroll
+      for (int d = 0; d < kScaleAhead; ++d)
+        if (d < kblocks) load_scales(blockIdx.x, d, ring_a[d], ring_b[d]);
+    }
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       const TileCoord tc = tile_coord(p, t);
       const int m_start = tc.mb * kBM + quarter * 32;
-      const int row = m_start + lane;
-      const bool row_ok = row < p.M;
-      const float* sa_col = p.a_scale + row;              // sa[j][row] at sa_col[j * M]
-      const float* sb_row = p.b_scale + static_cast<int64_t>(tc.nb) * kblocks;
       float acc[kBsCols];
 #pragma unroll
       for (int j = 0; j < kBsCols; ++j) acc[j] = 0.f;
-      float s_next = (row_ok ? __ldg(sa_col) : 0.f) * __ldg(sb_row);
-      for (int kb = 0; kb < kblocks; ++kb) {
-        const float s = s_next;
-        if (kb + 1 < kblocks)
-          s_next = (row_ok ? __ldg(sa_col + static_cast<int64_t>(kb + 1) * p.M) : 0.f) * __ldg(sb_row + kb + 1);
-        ok = mbar_wait(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + part * kBsBN + col0;
-        uint32_t v0[32], v1[32];
-        tmem_ld_32x32b_x32(taddr, v0);
-        tmem_ld_32x32b_x32(taddr + 32, v1);
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(pempty_bar(part));
+      for (int kb0 = 0; kb0 < kblocks && ok; kb0 += kScaleAhead) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = fmaf(__uint_as_float(v0[j]), s, acc[j]);
-          acc[32 + j] = fmaf(__uint_as_float(v1[j]), s, acc[32 + j]);
-        }
-        if (++part == kBsParts) {
-          part = 0;
-          ppar ^= 1;
+        for (int d = 0; d < kScaleAhead; ++d) {
+          const int kb = kb0 + d;
+          if (kb < kblocks) {
+            const float s = ring_a[d] * ring_b[d];
+            if (kb + kScaleAhead < kblocks) load_scales(t, kb + kScaleAhead, ring_a[d], ring_b[d]);
+            ok = mbar_wait(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + part * kBsBN + col0;
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(taddr, v0);
+            tmem_ld_32x32b_x32(taddr + 32, v1);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(pempty_bar(part));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              acc[j] = fmaf(__uint_as_float(v0[j]), s, acc[j]);
+              acc[32 + j] = fmaf(__uint_as_float(v1[j]), s, acc[32 + j]);
+            }
+            if (++part == kBsParts) {
+              part = 0;
+              ppar ^= 1;
+            }
+          }
         }
       }
       if (!ok) break;
+      // the next tile's first scales load while this tile is stored
+      const int tn = t + static_cast<int>(gridDim.x);
+      if (tn < p.num_tiles) {
+#pragma unroll
+        for (int d = 0; d < kScaleAhead; ++d)
+          if (d < kblocks) load_scales(tn, d, ring_a[d], ring_b[d]);
+      }
       const int n_start = tc.nb * kBsBN + col0;
       float f[32];
 #pragma unroll

@@ -248,27 +248,42 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 namespace {
 
 constexpr int kDenseBN = 256;
-constexpr int kDenseStages = 4;
-constexpr int kDenseEpiWarps = 4;
+// Two configurations: a long K loop wants a deep operand ring (4 stages); a
+// short one (K <= 512, at most 4 stages per tile) is bound by the epilogue, so
+// it trades a stage for 8 epilogue warps (two per TMEM lane quarter).
+constexpr int kShortKBlocks = 4;
 
-template <int MODE>
+template <int MODE, int STAGES, int EPI_WARPS>
 struct DenseKernel {
-  using L = DenseLayout<kDenseBN, kDenseStages, kDenseEpiWarps>;
-  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, kDenseStages, kDenseEpiWarps>;
-  static constexpr int kThreads = 64 + 32 * kDenseEpiWarps;
+  using L = DenseLayout<kDenseBN, STAGES, EPI_WARPS>;
+  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS>;
+  static constexpr int kThreads = 64 + 32 * EPI_WARPS;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+  }
 };
 
 template <int MODE>
-cudaError_t prepare_dense() {
-  return cudaFuncSetAttribute(DenseKernel<MODE>::fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DenseKernel<MODE>::L::kDynSmem);
+using LongK = DenseKernel<MODE, 4, 4>;
+template <int MODE>
+using ShortK = DenseKernel<MODE, 3, 8>;
+
+int dense_bk(int mode) { return mode == kModeBf16 ? 64 : 128; }
+
+bool short_k(int mode, int64_t K) { return (K + dense_bk(mode) - 1) / dense_bk(mode) <= kShortKBlocks; }
+
+template <typename Kern>
+sg_status_t launch_with(const LaunchArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const CUtensorMap& tmC, const GemmParams& p) {
+  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
+  Kern::fn<<<grid, Kern::kThreads, Kern::L::kDynSmem, a.stream>>>(tmA, tmB, tmC, p);
+  return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
 }
 
 template <int MODE>
 sg_status_t launch_dense_impl(const LaunchArgs& a) {
-  using K = DenseKernel<MODE>;
   const bool bf16 = (MODE == kModeBf16);
-  const int bk = bf16 ? 64 : 128;
+  const int bk = dense_bk(MODE);
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint64_t el = bf16 ? 2 : 1;
   CUtensorMap tmA, tmB, tmC;
@@ -290,9 +305,14 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
   p.b_scale = static_cast<const float*>(a.b_scale);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
-  K::fn<<<grid, K::kThreads, K::L::kDynSmem, a.stream>>>(tmA, tmB, tmC, p);
-  return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
+  return short_k(MODE, a.K) ? launch_with<ShortK<MODE>>(a, tmA, tmB, tmC, p)
+                            : launch_with<LongK<MODE>>(a, tmA, tmB, tmC, p);
+}
+
+template <int MODE>
+cudaError_t prepare_dense() {
+  cudaError_t e = LongK<MODE>::prepare();
+  return e == cudaSuccess ? ShortK<MODE>::prepare() : e;
 }
 
 }  // namespace
@@ -305,11 +325,11 @@ sg_status_t dense_launch(const LaunchArgs& a) {
   return a.mode == kModeBf16 ? launch_dense_impl<kModeBf16>(a) : launch_dense_impl<kModePtpc>(a);
 }
 
-void dense_config(int mode, TileConfig* c) {
+void dense_config(int mode, int64_t K, TileConfig* c) {
   c->bm = kBM;
   c->bn = kDenseBN;
-  c->bk = mode == kModeBf16 ? 64 : 128;
-  c->stages = kDenseStages;
+  c->bk = dense_bk(mode);
+  c->stages = short_k(mode, K) ? 3 : 4;
 }
 
 }  // namespace sg

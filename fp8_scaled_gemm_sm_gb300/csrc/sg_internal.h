@@ -42,7 +42,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
 
 cudaError_t dense_prepare(int mode);
 sg_status_t dense_launch(const LaunchArgs& a);
-void dense_config(int mode, TileConfig* c);
+void dense_config(int mode, int64_t K, TileConfig* c);
 
 cudaError_t mxfp8_prepare();
 sg_status_t mxfp8_launch(const LaunchArgs& a);
