@@ -37,8 +37,16 @@ bool debug_enabled() {
   return on;
 }
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 sg_status_t fail(sg_status_t s, const char* what) {
-  if (debug_enabled()) std::fprintf(stderr, "scaled_gemm: %s (%s)\n", what, scaled_gemm_status_string(s));
+  if (debug_enabled()) {
+    if (s == SG_ERR_CUDA && g_last_cuda_error != cudaSuccess)
+      std::fprintf(stderr, "scaled_gemm: %s (%s: %s)\n", what, scaled_gemm_status_string(s),
+                   cudaGetErrorString(g_last_cuda_error));
+    else
+      std::fprintf(stderr, "scaled_gemm: %s (%s)\n", what, scaled_gemm_status_string(s));
+  }
   return s;
 }
 
@@ -79,6 +87,9 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 }  // namespace
 
 namespace sg {
+
+void note_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+const char* last_cuda_error() { return cudaGetErrorString(g_last_cuda_error); }
 
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer,

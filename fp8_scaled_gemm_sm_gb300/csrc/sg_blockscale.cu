@@ -190,33 +190,46 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     // Scale products s = sa[j][row] * sb[nb][j] are loaded kScaleAhead K blocks
     // before they are needed (a ring of registers), and the first ones of the next
     // tile are loaded before this tile's epilogue, so no promotion step waits on
-    // a global load.
+    // a global load.  The accumulator is 32 packed fp32 pairs, updated with one
+    // f32x2 FMA per pair.
     constexpr int kScaleAhead = 4;
     float ring_a[kScaleAhead], ring_b[kScaleAhead];
-    auto load_scales = [&](int t, int kb, float& sa_out, float& sb_out) {
+    const float* sa_base = p.a_scale;
+    const float* sb_base = p.b_scale;
+    bool row_ok = false;
+    auto tile_scale_ptrs = [&](int t, const float*& sa_ptr, const float*& sb_ptr) {
       const TileCoord c = tile_coord(p, t);
       const int row = c.mb * kBM + quarter * 32 + lane;
-      sa_out = row < p.M ? __ldg(p.a_scale + static_cast<int64_t>(kb) * p.M + row) : 0.f;
-      sb_out = __ldg(p.b_scale + static_cast<int64_t>(c.nb) * kblocks + kb);
+      row_ok = row < p.M;
+      sa_ptr = sa_base + (row_ok ? row : 0);
+      sb_ptr = sb_base + static_cast<int64_t>(c.nb) * kblocks;
+    };
+    const float* sa_ptr = sa_base;
+    const float* sb_ptr = sb_base;
+    auto load_scales = [&](int kb, float& a_out, float& b_out) {
+      a_out = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.M) : 0.f;
+      b_out = __ldg(sb_ptr + kb);
     };
     if (static_cast<int>(blockIdx.x) < p.num_tiles) {
+      tile_scale_ptrs(blockIdx.x, sa_ptr, sb_ptr);
 #pragma unroll
       for (int d = 0; d < kScaleAhead; ++d)
-        if (d < kblocks) load_scales(blockIdx.x, d, ring_a[d], ring_b[d]);
+        if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
     }
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       const TileCoord tc = tile_coord(p, t);
       const int m_start = tc.mb * kBM + quarter * 32;
-      float acc[kBsCols];
+      uint64_t acc[kBsCols / 2];
 #pragma unroll
-      for (int j = 0; j < kBsCols; ++j) acc[j] = 0.f;
+      for (int j = 0; j < kBsCols / 2; ++j) acc[j] = 0;
       for (int kb0 = 0; kb0 < kblocks && ok; kb0 += kScaleAhead) {
 #pragma unroll
         for (int d = 0; d < kScaleAhead; ++d) {
           const int kb = kb0 + d;
           if (kb < kblocks) {
-            const float s = ring_a[d] * ring_b[d];
-            if (kb + kScaleAhead < kblocks) load_scales(t, kb + kScaleAhead, ring_a[d], ring_b[d]);
+            const float sc = ring_a[d] * ring_b[d];
+            const uint64_t s2 = pack_f32x2(__float_as_uint(sc), __float_as_uint(sc));
+            if (kb + kScaleAhead < kblocks) load_scales(kb + kScaleAhead, ring_a[d], ring_b[d]);
             ok = mbar_wait(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
             if (!__all_sync(0xffffffffu, ok)) {
               ok = false;
@@ -232,9 +245,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             tc_fence_before();
             mbar_arrive(pempty_bar(part));
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[j] = fmaf(__uint_as_float(v0[j]), s, acc[j]);
-              acc[32 + j] = fmaf(__uint_as_float(v1[j]), s, acc[32 + j]);
+            for (int j = 0; j < 16; ++j) {
+              acc[j] = fma_f32x2(pack_f32x2(v0[2 * j], v0[2 * j + 1]), s2, acc[j]);
+              acc[16 + j] = fma_f32x2(pack_f32x2(v1[2 * j], v1[2 * j + 1]), s2, acc[16 + j]);
             }
             if (++part == kBsParts) {
               part = 0;
@@ -247,18 +260,23 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       // the next tile's first scales load while this tile is stored
       const int tn = t + static_cast<int>(gridDim.x);
       if (tn < p.num_tiles) {
+        tile_scale_ptrs(tn, sa_ptr, sb_ptr);
 #pragma unroll
         for (int d = 0; d < kScaleAhead; ++d)
-          if (d < kblocks) load_scales(tn, d, ring_a[d], ring_b[d]);
+          if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
       }
       const int n_start = tc.nb * kBsBN + col0;
-      float f[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) f[j] = acc[j];
-      store_box32(bufs, box, f, &tmC, n_start, m_start, p.N, p.M, lane);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t packed[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) f[j] = acc[32 + j];
-      store_box32(bufs, box, f, &tmC, n_start + 32, m_start, p.N, p.M, lane);
+        for (int j = 0; j < 16; ++j) {
+          float lo, hi;
+          unpack_f32x2(acc[16 * h + j], lo, hi);
+          packed[j] = pack_bf16x2(lo, hi);
+        }
+        store_box32(bufs, box, packed, &tmC, n_start + 32 * h, m_start, p.N, p.M, lane);
+      }
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -304,7 +322,7 @@ sg_status_t blockscale_launch(const LaunchArgs& a) {
   p.timeout_ns = a.timeout_ns;
   const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
   blockscale_gemm_kernel<<<grid, kBsThreads, BsLayout::kDynSmem, a.stream>>>(tmA, tmB, tmC, p);
-  return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
+  return launch_status();
 }
 
 void blockscale_config(TileConfig* c) {

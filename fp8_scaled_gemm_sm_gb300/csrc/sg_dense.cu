@@ -35,14 +35,14 @@
 
 namespace sg {
 
-template <int BN, int STAGES, int EPI_WARPS>
+template <int BN, int STAGES, int EPI_WARPS, int NBOX, int BOXW>
 struct DenseLayout {
   static constexpr int kAStage = kBM * kRowBytes;
   static constexpr int kBStage = BN * kRowBytes;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kAStage;
   static constexpr int kOffC = kOffB + STAGES * kBStage;
-  static constexpr int kOffScale = kOffC + EPI_WARPS * 2 * kCBoxBytes;  // per-warp column scales
+  static constexpr int kOffScale = kOffC + EPI_WARPS * NBOX * cbox_bytes<BOXW>();  // per-warp column scales
   static constexpr int kScaleCols = BN * 4 / EPI_WARPS;                   // columns per warp
   static constexpr int kOffBar = kOffScale + EPI_WARPS * kScaleCols * 4;
   static constexpr int kNumBars = 2 * STAGES + 5;
@@ -52,12 +52,12 @@ struct DenseLayout {
   static_assert(kOffC % 1024 == 0, "store boxes need 512-byte alignment");
 };
 
-template <int MODE, int BN, int STAGES, int EPI_WARPS>
+template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using L = DenseLayout<BN, STAGES, EPI_WARPS>;
+  using L = DenseLayout<BN, STAGES, EPI_WARPS, NBOX, BOXW>;
   constexpr bool kScaled = (MODE == kModePtpc);
   constexpr int kBK = (MODE == kModeBf16) ? 64 : 128;       // K elements per stage
   constexpr int kUmmaK = (MODE == kModeBf16) ? 16 : 32;      // K per tcgen05.mma
@@ -68,8 +68,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   constexpr uint32_t kTmemCols = 512;
   constexpr int kAccStride = 256;
   constexpr int kColsPerWarp = BN * 4 / EPI_WARPS;
+  constexpr int kBRowsPerCta = BN / CLUSTER;                 // B rows each CTA loads
+  constexpr uint16_t kClusterMask = (1u << CLUSTER) - 1;
   static_assert(BN <= 256 && BN % 64 == 0, "BN");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+  static_assert(CLUSTER == 1 || CLUSTER == 2, "cluster size");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -88,11 +91,24 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Cluster of CLUSTER CTAs on vertically adjacent tiles (same N block): each CTA
+  // loads BN / CLUSTER rows of the shared B tile and multicasts them to all.
+  const int rank = CLUSTER > 1 ? static_cast<int>(cluster_cta_rank()) : 0;
+  const int group = CLUSTER > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int ngroups = CLUSTER > 1 ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+  const int num_group_tiles = ((p.m_blocks + CLUSTER - 1) / CLUSTER) * p.n_blocks;
+  auto coord = [&](int tg) {
+    TileCoord c;
+    const int mg = tg / p.n_blocks;
+    c.nb = tg - mg * p.n_blocks;
+    c.mb = mg * CLUSTER + rank;
+    return c;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CLUSTER);  // one MMA commit from every CTA that reads the stage's B
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -108,6 +124,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CLUSTER > 1) cluster_sync();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
@@ -120,8 +137,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       int stage = 0, kstep = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(p, t);
+      for (int tg = group; tg < num_group_tiles && ok; tg += ngroups) {
+        const TileCoord tc = coord(tg);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
             ok = false;
@@ -130,7 +147,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           if (kstep != p.skip_kstep) {
             mbar_arrive_expect_tx(full_bar(stage), kTx);
             tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
-            tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN, full_bar(stage));
+            if constexpr (CLUSTER > 1)
+              tma_load_2d_multicast(sB + stage * L::kBStage + rank * kBRowsPerCta * kRowBytes, &tmB,
+                                    kb * kBK, tc.nb * BN + rank * kBRowsPerCta, full_bar(stage),
+                                    kClusterMask);
+            else
+              tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN, full_bar(stage));
             issued |= 1u << stage;
             last_par[stage] = phase;
           }
@@ -143,6 +165,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       if (!ok) {  // loads still in flight must land before the CTA can exit
         for (int s = 0; s < STAGES; ++s)
           if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+      } else if (CLUSTER > 1) {
+        // Every peer's MMA commit to this CTA's empty barriers must have landed
+        // before the CTA exits: wait for the release of each stage's last fill.
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
       }
     }
   } else if (warp == 1) {
@@ -151,7 +178,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+      for (int tg = group; tg < num_group_tiles && ok; tg += ngroups, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
         if (!mbar_wait(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
@@ -177,7 +204,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             else
               mma_f8f6f4(d, ad, bd, kIdesc, (kb | k) != 0);
           }
-          mma_commit(empty_bar(stage));
+          // The stage is free once every CTA that received its B half has read it.
+          if constexpr (CLUSTER > 1)
+            mma_commit_multicast(empty_bar(stage), kClusterMask);
+          else
+            mma_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -196,12 +227,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     const int ew = warp - 2;          // 0 .. EPI_WARPS-1
     const int quarter = warp & 3;     // TMEM lanes this warp may access
     const int col0 = (ew >> 2) * kColsPerWarp;
-    const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
+    const uint32_t bufs = sC + ew * NBOX * cbox_bytes<BOXW>();
     float* col_scale = reinterpret_cast<float*>(smem + L::kOffScale) + ew * kColsPerWarp;
     int it = 0;
     uint32_t box = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(p, t);
+    for (int tg = group; tg < num_group_tiles; tg += ngroups, ++it) {
+      const TileCoord tc = coord(tg);
       const int acc = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
       const int m_start = tc.mb * kBM + quarter * 32;
@@ -222,11 +253,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              acc * kAccStride + col0;
-      epilogue_tile<kColsPerWarp, kScaled>(taddr, bufs, box, col_scale, row_scale, &tmC, n_start,
-                                          m_start, p.N, p.M, lane, [&]() {
-                                            tc_fence_before();
-                                            mbar_arrive(tempty_bar(acc));
-                                          });
+      epilogue_tile<kColsPerWarp, kScaled, NBOX, BOXW>(taddr, bufs, box, col_scale, row_scale, &tmC,
+                                                 n_start, m_start, p.N, p.M, lane, [&]() {
+                                                   tc_fence_before();
+                                                   mbar_arrive(tempty_bar(acc));
+                                                 });
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -235,6 +266,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if constexpr (CLUSTER > 1) cluster_sync();  // no CTA leaves while a peer may still signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -253,20 +285,23 @@ constexpr int kDenseBN = 256;
 // it trades a stage for 8 epilogue warps (two per TMEM lane quarter).
 constexpr int kShortKBlocks = 4;
 
-template <int MODE, int STAGES, int EPI_WARPS>
+template <int MODE, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW>
 struct DenseKernel {
-  using L = DenseLayout<kDenseBN, STAGES, EPI_WARPS>;
-  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS>;
+  using L = DenseLayout<kDenseBN, STAGES, EPI_WARPS, NBOX, BOXW>;
+  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX, CLUSTER, BOXW>;
+  static constexpr int kBoxW = BOXW;
   static constexpr int kThreads = 64 + 32 * EPI_WARPS;
+  static constexpr int kCluster = CLUSTER;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
   }
 };
 
+// Pairs of CTAs on vertically adjacent tiles share (multicast) each B tile.
 template <int MODE>
-using LongK = DenseKernel<MODE, 4, 4>;
+using LongK = DenseKernel<MODE, 4, 4, 2, 2, 32>;
 template <int MODE>
-using ShortK = DenseKernel<MODE, 3, 8>;
+using ShortK = DenseKernel<MODE, 3, 8, 2, 2, 32>;
 
 int dense_bk(int mode) { return mode == kModeBf16 ? 64 : 128; }
 
@@ -274,10 +309,35 @@ bool short_k(int mode, int64_t K) { return (K + dense_bk(mode) - 1) / dense_bk(m
 
 template <typename Kern>
 sg_status_t launch_with(const LaunchArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                        const CUtensorMap& tmC, const GemmParams& p) {
-  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
-  Kern::fn<<<grid, Kern::kThreads, Kern::L::kDynSmem, a.stream>>>(tmA, tmB, tmC, p);
-  return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
+                        const GemmParams& p) {
+  constexpr int cl = Kern::kCluster;
+  constexpr int bw = Kern::kBoxW;
+  CUtensorMap tmC;
+  if (!encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, bw, kCBoxRows,
+                 bw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+    return SG_ERR_CUDA;
+  const int group_tiles = ((p.m_blocks + cl - 1) / cl) * p.n_blocks;
+  const int max_groups = a.num_sms / cl;
+  const int groups = group_tiles < max_groups ? group_tiles : max_groups;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * cl, 1, 1);
+  cfg.blockDim = dim3(Kern::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Kern::L::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, Kern::fn, tmA, tmB, tmC, p);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    cudaGetLastError();  // clear the non-sticky launch error
+    return SG_ERR_CUDA;
+  }
+  return SG_OK;
 }
 
 template <int MODE>
@@ -286,11 +346,11 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
   const int bk = dense_bk(MODE);
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint64_t el = bf16 ? 2 : 1;
-  CUtensorMap tmA, tmB, tmC;
+  static_assert(LongK<MODE>::kCluster == ShortK<MODE>::kCluster, "one B tensor map for both");
+  CUtensorMap tmA, tmB;
   if (!encode_2d(&tmA, dt, a.A, a.K, a.M, a.K * el, bk, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, kDenseBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols,
-                 kCBoxRows, CU_TENSOR_MAP_SWIZZLE_64B))
+      !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, kDenseBN / LongK<MODE>::kCluster,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return SG_ERR_CUDA;
   GemmParams p{};
   p.M = static_cast<int32_t>(a.M);
@@ -305,8 +365,8 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
   p.b_scale = static_cast<const float*>(a.b_scale);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  return short_k(MODE, a.K) ? launch_with<ShortK<MODE>>(a, tmA, tmB, tmC, p)
-                            : launch_with<LongK<MODE>>(a, tmA, tmB, tmC, p);
+  return short_k(MODE, a.K) ? launch_with<ShortK<MODE>>(a, tmA, tmB, p)
+                            : launch_with<LongK<MODE>>(a, tmA, tmB, p);
 }
 
 template <int MODE>

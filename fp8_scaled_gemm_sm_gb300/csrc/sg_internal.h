@@ -40,6 +40,18 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
                uint64_t outer, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swizzle);
 
+// Remember a CUDA error from a kernel launch for SG_DEBUG reporting (per thread).
+void note_cuda_error(cudaError_t e);
+const char* last_cuda_error();
+
+// cudaGetLastError after a launch, noted; SG_OK or SG_ERR_CUDA.
+inline sg_status_t launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return SG_OK;
+  note_cuda_error(e);
+  return SG_ERR_CUDA;
+}
+
 cudaError_t dense_prepare(int mode);
 sg_status_t dense_launch(const LaunchArgs& a);
 void dense_config(int mode, int64_t K, TileConfig* c);

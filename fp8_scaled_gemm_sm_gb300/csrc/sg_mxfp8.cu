@@ -15,13 +15,14 @@
 //              [4 K-blocks][128 m], sb rows [4][224 n], K-block major as they
 //              sit in memory) into stage s; one full[s] barrier covers all four.
 //   warp 1     TMEM owner and MMA issuer.  Per stage: wait sf_ready[s], copy the
-//              stage's scale factors shared -> TMEM with tcgen05.cp (32x128b,
-//              warpx4), then 4 block-scaled MMAs (K = 32 each, scale-factor id k
-//              selects the k-th byte of each 32-bit scale word), commit empty[s].
+//              stage's scale factors shared -> TMEM with two tcgen05.cp (128x128b
+//              for A, 128x256b for B's two 128-row chunks), then 4 block-scaled
+//              MMAs (K = 32 each, scale-factor id k selects the k-th byte of each
+//              32-bit scale word), commit empty[s].
 //   warp 2     scale-factor warp: wait full[s], regroup the raw bytes into the
-//              layout tcgen05.cp expects (row r of a 128-row chunk holds the four
-//              32-bit words for rows r, r+32, r+64, r+96, each word the four
-//              K-block scales of that row), fence the async proxy, arrive
+//              layout the MMA reads (in every 32-lane quarter, lane r column c
+//              holds the word for row 32 c + r of a 128-row chunk, each word the
+//              four K-block scales of that row), fence the async proxy, arrive
 //              sf_ready[s].  Its fence also orders its generic reads of the raw
 //              boxes before the TMA refill of stage s (deepseek-ai/DeepGEMM PR 453,
 //              Fix).
@@ -50,8 +51,8 @@ struct MxLayout {
   static constexpr int kBStage = kMxBN * kRowBytes;      // 28 KB
   static constexpr int kRawA = 4 * kBM;                  // [4][128] e8m0
   static constexpr int kRawB = 4 * kMxBN;                // [4][224] e8m0
-  static constexpr int kSfA = 512;                       // one 128-row chunk
-  static constexpr int kSfB = 1024;                      // two 128-row chunks
+  static constexpr int kSfA = 2048;                      // 128 lanes x 16 B
+  static constexpr int kSfB = 4096;                      // 128 lanes x 32 B
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kMxStages * kAStage;
   static constexpr int kOffC = kOffB + kMxStages * kBStage;
@@ -74,17 +75,28 @@ struct MxLayout {
 __device__ __forceinline__ uint32_t sf_col_a(int s) { return s < 2 ? 224 + 12 * s : 480 + 12 * (s - 2); }
 __device__ __forceinline__ uint32_t sf_col_b(int s) { return sf_col_a(s) + 4; }
 
-// Descriptor of one 128-row scale chunk for tcgen05.cp 32x128b: 32 rows of 16
-// bytes, no swizzle, 8-row core matrices 128 bytes apart.
-__device__ __forceinline__ uint64_t sf_chunk_desc(uint32_t addr) { return smem_desc(addr, 0, 128, 0); }
+// Scale factors go to TMEM with two copies per stage: tcgen05.cp.128x128b for A
+// (lane l, columns 0-3) and tcgen05.cp.128x256b for B (lane l, columns 0-7).
+// For a 128-row chunk the MMA takes, in every 32-lane quarter, lane r and column
+// c to hold the four K-block scales (bytes 0-3) of row 32 c + r of the chunk.
+// The shared-memory source is therefore the same 16 (A) or 32 (B) bytes for
+// lanes r, r+32, r+64, r+96, laid out in 8-row x 16-byte core matrices:
+// row l, 16-byte chunk j at (l / 8) * SBO + j * LBO + (l % 8) * 16.
+__device__ __forceinline__ uint64_t sf_desc_a(uint32_t addr) { return smem_desc(addr, 0, 128, 0); }
+__device__ __forceinline__ uint64_t sf_desc_b(uint32_t addr) { return smem_desc(addr, 128, 256, 0); }
 
-// Regroup one 128-row chunk of raw K-block-major scales into the tcgen05.cp
-// layout: lane r writes 16 bytes at chunk + 16 r, word w = the 4 K-block scales
-// of row 32 w + r.  `pitch` is the raw box row length, `rows_valid` the rows of
-// the raw box that exist (later rows read as 0).
-__device__ __forceinline__ void regroup_sf_chunk(const uint8_t* raw, int pitch, int row0, int rows_valid,
-                                                 uint32_t chunk, int lane) {
-  uint32_t w[4];
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// The four 32-bit scale words lane r contributes for a 128-row chunk starting at
+// row0 of a raw K-block-major box ([4 K blocks][pitch] e8m0 bytes): word w holds
+// the 4 K-block scales of row row0 + 32 w + r (0 past rows_valid).
+__device__ __forceinline__ void sf_words(const uint8_t* raw, int pitch, int row0, int rows_valid, int lane,
+                                         uint32_t (&w)[4]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int row = row0 + 32 * q + lane;
@@ -95,7 +107,6 @@ __device__ __forceinline__ void regroup_sf_chunk(const uint8_t* raw, int pitch, 
     }
     w[q] = v;
   }
-  st_shared_v4(chunk + 16 * lane, w[0], w[1], w[2], w[3]);
 }
 
 __global__ void __launch_bounds__(kMxThreads, 1)
@@ -218,9 +229,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           tc_fence_after();
           const uint32_t tsa = tmem_base + sf_col_a(stage);
           const uint32_t tsb = tmem_base + sf_col_b(stage);
-          tmem_cp_32x128b_warpx4(tsa, sf_chunk_desc(sSfA + stage * L::kSfA));
-          tmem_cp_32x128b_warpx4(tsb, sf_chunk_desc(sSfB + stage * L::kSfB));
-          tmem_cp_32x128b_warpx4(tsb + 4, sf_chunk_desc(sSfB + stage * L::kSfB + 512));
+          tmem_cp_128x128b(tsa, sf_desc_a(sSfA + stage * L::kSfA));
+          tmem_cp_128x256b(tsb, sf_desc_b(sSfB + stage * L::kSfB));
           const uint32_t a0 = sA + stage * L::kAStage;
           const uint32_t b0 = sB + stage * L::kBStage;
 #pragma unroll
@@ -256,9 +266,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         const uint8_t* rawA = smem + L::kOffRawA + stage * L::kRawA;
         const uint8_t* rawB = smem + L::kOffRawB + stage * L::kRawB;
-        regroup_sf_chunk(rawA, kBM, 0, kBM, sSfA + stage * L::kSfA, lane);
-        regroup_sf_chunk(rawB, kMxBN, 0, kMxBN, sSfB + stage * L::kSfB, lane);
-        regroup_sf_chunk(rawB, kMxBN, 128, kMxBN, sSfB + stage * L::kSfB + 512, lane);
+        uint32_t wa[4], wb0[4], wb1[4];
+        sf_words(rawA, kBM, 0, kBM, lane, wa);
+        sf_words(rawB, kMxBN, 0, kMxBN, lane, wb0);
+        sf_words(rawB, kMxBN, 128, kMxBN, lane, wb1);
+        const uint32_t dA = sSfA + stage * L::kSfA;
+        const uint32_t dB = sSfB + stage * L::kSfB;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // the same words for lanes r + 32 q
+          const int l = 32 * q + lane;
+          st_shared_v4(dA + (l >> 3) * 128 + (l & 7) * 16, wa[0], wa[1], wa[2], wa[3]);
+          st_shared_v4(dB + (l >> 3) * 256 + (l & 7) * 16, wb0[0], wb0[1], wb0[2], wb0[3]);
+          st_shared_v4(dB + (l >> 3) * 256 + 128 + (l & 7) * 16, wb1[0], wb1[1], wb1[2], wb1[3]);
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(sf_bar(stage));
@@ -340,7 +360,7 @@ sg_status_t mxfp8_launch(const LaunchArgs& a) {
   p.timeout_ns = a.timeout_ns;
   const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
   mxfp8_gemm_kernel<<<grid, kMxThreads, MxLayout::kDynSmem, a.stream>>>(tmA, tmB, tmSA, tmSB, tmC, p);
-  return cudaGetLastError() == cudaSuccess ? SG_OK : SG_ERR_CUDA;
+  return launch_status();
 }
 
 void mxfp8_config(TileConfig* c) {
