@@ -274,6 +274,250 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Pair kernel: two CTAs on neighbouring SMs compute one 256 x BN tile with
+// tcgen05.mma.cta_group::2.  Each CTA stages its own 128 rows of A and its half
+// (BN/2 rows) of B, so per SM the shared-memory operand traffic per FLOP is that
+// of a 128 x 2BN tile; the even CTA of the pair issues the MMAs, the TMA bytes
+// of both CTAs complete its full[s] barrier, its commits arrive on both CTAs'
+// empty[s] and tmem_full[acc], and both CTAs' epilogues release the accumulator
+// on its tmem_empty[acc].  Each CTA reads its own 128 accumulator rows.
+// ---------------------------------------------------------------------------
+
+template <int BN, int STAGES, int EPI_WARPS, int NBOX>
+struct PairLayout {
+  static constexpr int kAStage = kBM * kRowBytes;
+  static constexpr int kBStage = (BN / 2) * kRowBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + STAGES * kAStage;
+  static constexpr int kOffC = kOffB + STAGES * kBStage;
+  static constexpr int kColsPerWarp = BN * 4 / EPI_WARPS;
+  static constexpr int kOffScale = kOffC + EPI_WARPS * NBOX * kCBoxBytes;
+  static constexpr int kOffBar = kOffScale + EPI_WARPS * kColsPerWarp * 4;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16 + 4 * STAGES;
+  static constexpr int kDynSmem = kBytes + 1024;
+  static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "alignment");
+};
+
+template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX>
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
+    dense_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  using L = PairLayout<BN, STAGES, EPI_WARPS, NBOX>;
+  constexpr bool kScaled = (MODE == kModePtpc);
+  constexpr int kBK = (MODE == kModeBf16) ? 64 : 128;
+  constexpr int kUmmaK = (MODE == kModeBf16) ? 16 : 32;
+  constexpr int kKSteps = kBK / kUmmaK;
+  constexpr uint32_t kIdesc =
+      (MODE == kModeBf16) ? instr_desc(1, 1, 2 * kBM, BN) : instr_desc(0, 0, 2 * kBM, BN);
+  constexpr uint32_t kTxPair = 2 * (L::kAStage + L::kBStage);  // both CTAs' bytes
+  constexpr uint32_t kTmemCols = 512;
+  constexpr int kAccStride = 256;
+  constexpr int kColsPerWarp = L::kColsPerWarp;
+  constexpr uint16_t kBoth = 0x3;
+  static_assert(BN <= 256 && BN % 64 == 0, "BN");
+  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA = smem_addr(smem + L::kOffA);
+  const uint32_t sB = smem_addr(smem + L::kOffB);
+  const uint32_t sC = smem_addr(smem + L::kOffC);
+  const uint32_t bar0 = smem_addr(smem + L::kOffBar);
+  auto full_bar = [&](int s) { return bar0 + 8 * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8 * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  uint32_t* last_par = misc + 4;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_cta_rank());
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
+  const int num_pair_tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
+  auto coord = [&](int tp) {
+    TileCoord c;
+    const int mp = tp / p.n_blocks;
+    c.nb = tp - mp * p.n_blocks;
+    c.mb = 2 * mp + rank;  // this CTA's 128-row block
+    return c;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);   // the leader's producer arms it for both CTAs' bytes
+      mbar_init(empty_bar(s), 1);  // one pair commit per round
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * 32 * EPI_WARPS);  // both CTAs' epilogue threads
+    }
+    mbar_init(drain_bar, 1);
+    misc[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {  // one warp in each CTA of the pair allocates together
+    tmem_alloc_pair(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0, kstep = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
+        const TileCoord tc = coord(tp);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
+          if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (kstep != p.skip_kstep) {
+            const uint32_t fb = map_to_cta(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
+            tma_load_2d_pair(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
+            tma_load_2d_pair(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN + rank * (BN / 2), fb);
+            issued |= 1u << stage;
+            last_par[stage] = phase;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        if (leader) {
+          for (int s = 0; s < STAGES; ++s)
+            if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+        } else {
+          // this CTA's loads complete on the leader's barrier: give them time to land
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 2000000ull) {
+          }
+        }
+      } else {
+        // every pair commit to this CTA's empty barriers must land before exit
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- pair MMA issuer (leader only) ----------------
+    if (lane == 0 && leader) {
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!mbar_wait_cluster(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccStride;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait_cluster(full_bar(stage), phase, wd, kWhereMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sA + stage * L::kAStage;
+          const uint32_t b0 = sB + stage * L::kBStage;
+#pragma unroll
+          for (int k = 0; k < kKSteps; ++k) {
+            const uint64_t ad = kmajor_sw128_desc(a0 + k * kUmmaK * (kRowBytes / kBK));
+            const uint64_t bd = kmajor_sw128_desc(b0 + k * kUmmaK * (kRowBytes / kBK));
+            if constexpr (MODE == kModeBf16)
+              mma_f16_pair(d, ad, bd, kIdesc, (kb | k) != 0);
+            else
+              mma_f8f6f4_pair(d, ad, bd, kIdesc, (kb | k) != 0);
+          }
+          mma_commit_pair(empty_bar(stage), kBoth);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull_bar(acc), kBoth);
+      }
+      if (!ok) {
+        mma_commit_pair(drain_bar, 0x1);
+        mbar_wait_drain(drain_bar, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int col0 = (ew >> 2) * kColsPerWarp;
+    const uint32_t bufs = sC + ew * NBOX * kCBoxBytes;
+    float* col_scale = reinterpret_cast<float*>(smem + L::kOffScale) + ew * kColsPerWarp;
+    int it = 0;
+    uint32_t box = 0;
+    for (int tp = pair; tp < num_pair_tiles; tp += npairs, ++it) {
+      const TileCoord tc = coord(tp);
+      const int acc = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      const int m_start = tc.mb * kBM + quarter * 32;
+      const int n_start = tc.nb * BN + col0;
+      float row_scale = 0.f;
+      if constexpr (kScaled) {
+        __syncwarp();
+        for (int i = lane; i < kColsPerWarp; i += 32) {
+          const int n = n_start + i;
+          col_scale[i] = (n < p.N) ? p.b_scale[n] : 0.f;
+        }
+        const int row = m_start + lane;
+        row_scale = (row < p.M) ? p.a_scale[row] : 0.f;
+        __syncwarp();
+      }
+      const bool ok = mbar_wait_cluster(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             acc * kAccStride + col0;
+      const uint32_t release_bar = map_to_cta(tempty_bar(acc), 0);
+      epilogue_tile<kColsPerWarp, kScaled, NBOX>(taddr, bufs, box, col_scale, row_scale, &tmC,
+                                                 n_start, m_start, p.N, p.M, lane, [&]() {
+                                                   tc_fence_before();
+                                                   mbar_arrive_cluster(release_bar);
+                                                 });
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal it or use its TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -290,6 +534,7 @@ struct DenseKernel {
   using L = DenseLayout<kDenseBN, STAGES, EPI_WARPS, NBOX, BOXW>;
   static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX, CLUSTER, BOXW>;
   static constexpr int kBoxW = BOXW;
+  static constexpr bool kPair = false;
   static constexpr int kThreads = 64 + 32 * EPI_WARPS;
   static constexpr int kCluster = CLUSTER;
   static cudaError_t prepare() {
@@ -297,9 +542,23 @@ struct DenseKernel {
   }
 };
 
-// Pairs of CTAs on vertically adjacent tiles share (multicast) each B tile.
+template <int MODE, int STAGES, int EPI_WARPS, int NBOX>
+struct PairKernel {
+  using L = PairLayout<kDenseBN, STAGES, EPI_WARPS, NBOX>;
+  static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX>;
+  static constexpr int kThreads = 64 + 32 * EPI_WARPS;
+  static constexpr int kCluster = 2;
+  static constexpr int kBoxW = 32;
+  static constexpr bool kPair = true;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+  }
+};
+
+// Long K: pair MMA (cta_group::2) on 256 x 256 tiles.  Short K: pairs of CTAs on
+// vertically adjacent 128 x 256 tiles that share (multicast) each B tile.
 template <int MODE>
-using LongK = DenseKernel<MODE, 4, 4, 2, 2, 32>;
+using LongK = PairKernel<MODE, 6, 4, 2>;
 template <int MODE>
 using ShortK = DenseKernel<MODE, 3, 8, 2, 2, 32>;
 
@@ -312,11 +571,12 @@ sg_status_t launch_with(const LaunchArgs& a, const CUtensorMap& tmA, const CUten
                         const GemmParams& p) {
   constexpr int cl = Kern::kCluster;
   constexpr int bw = Kern::kBoxW;
+  constexpr int rows_per_group = Kern::kPair ? 2 * kBM : kBM * cl;
   CUtensorMap tmC;
   if (!encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, bw, kCBoxRows,
                  bw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
     return SG_ERR_CUDA;
-  const int group_tiles = ((p.m_blocks + cl - 1) / cl) * p.n_blocks;
+  const int group_tiles = static_cast<int>((a.M + rows_per_group - 1) / rows_per_group) * p.n_blocks;
   const int max_groups = a.num_sms / cl;
   const int groups = group_tiles < max_groups ? group_tiles : max_groups;
   cudaLaunchConfig_t cfg = {};
