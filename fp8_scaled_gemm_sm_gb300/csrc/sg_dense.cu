@@ -558,7 +558,7 @@ struct PairKernel {
 // Long K: pair MMA (cta_group::2) on 256 x 256 tiles.  Short K: pairs of CTAs on
 // vertically adjacent 128 x 256 tiles that share (multicast) each B tile.
 template <int MODE>
-using LongK = PairKernel<MODE, 6, 4, 2>;
+using LongK = PairKernel<MODE, 5, 8, 2>;
 template <int MODE>
 using ShortK = DenseKernel<MODE, 3, 8, 2, 2, 32>;
 
