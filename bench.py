@@ -374,9 +374,10 @@ def run_e2e(work, launch, stream, args, control, dev):
     """The suite end to end through the C ABI with pinned host buffers.
 
     Per step and workload: H2D copy of its inputs, the GEMM, D2H copy of its C.
-    Three streams overlap the copies of one workload with the GEMMs of its
-    neighbours; events keep each workload's device buffers from being refilled
-    (or its C overwritten) before the previous use has finished.
+    Copy streams (each copy split over `--e2e-split` of them, so several copy
+    engines work at once) overlap the copies of one workload with the GEMMs of
+    its neighbours; events keep each workload's device buffers from being
+    refilled (or its C overwritten) before the previous use has finished.
     """
     steps = max(1, args.e2e_steps)
     host_in, host_out = [], []
@@ -396,50 +397,65 @@ def run_e2e(work, launch, stream, args, control, dev):
         host_out.append(torch.empty(d["C"].shape, dtype=d["C"].dtype, pin_memory=True))
         d2h += d["C"].numel() * d["C"].element_size()
     torch.cuda.synchronize()
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    nsplit = max(1, args.e2e_split)
+    s_in = [torch.cuda.Stream(dev) for _ in range(nsplit)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(nsplit)]
     n = len(work)
-    ev = lambda: torch.cuda.Event()  # noqa: E731
     in_done, gemm_done, out_done = [None] * n, [None] * n, [None] * n
+
+    def chunks(t):
+        flat = t.view(-1)
+        step_ = (flat.numel() + nsplit - 1) // nsplit
+        return [flat[j * step_:(j + 1) * step_] for j in range(nsplit)]
 
     def step():
         for i, (d, ins, out) in enumerate(zip(work, host_in, host_out)):
-            with torch.cuda.stream(s_in):
-                if gemm_done[i] is not None:
-                    s_in.wait_event(gemm_done[i])  # previous GEMM i has read its inputs
-                for key, h in zip(("A", "B", "sa", "sb"), ins):
-                    if h is not None:
-                        d[key].copy_(h, non_blocking=True)
-                in_done[i] = ev()
-                in_done[i].record(s_in)
+            # inputs: every tensor split over the copy streams
+            done = []
+            for j, q in enumerate(s_in):
+                with torch.cuda.stream(q):
+                    if gemm_done[i] is not None:
+                        q.wait_event(gemm_done[i])  # previous GEMM i has read its inputs
+                    for key, h in zip(("A", "B", "sa", "sb"), ins):
+                        if h is not None:
+                            chunks(d[key])[j].copy_(chunks(h)[j], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(q)
+                    done.append(e)
+            in_done[i] = done
             with torch.cuda.stream(stream):
-                stream.wait_event(in_done[i])
-                if out_done[i] is not None:
-                    stream.wait_event(out_done[i])  # previous C i has been copied out
+                for e in in_done[i]:
+                    stream.wait_event(e)
+                for e in out_done[i] or []:
+                    stream.wait_event(e)  # previous C i has been copied out
                 launch(d)
-                gemm_done[i] = ev()
+                gemm_done[i] = torch.cuda.Event()
                 gemm_done[i].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(gemm_done[i])
-                out.copy_(d["C"], non_blocking=True)
-                out_done[i] = ev()
-                out_done[i].record(s_out)
+            done = []
+            for j, q in enumerate(s_out):
+                with torch.cuda.stream(q):
+                    q.wait_event(gemm_done[i])
+                    chunks(out)[j].copy_(chunks(d["C"])[j], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(q)
+                    done.append(e)
+            out_done[i] = done
 
     step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     control.barrier()
     torch.cuda.synchronize()
-    e0.record(s_in)
-    s_out.wait_event(e0)
-    stream.wait_event(e0)
+    e0.record(stream)
+    for q in s_in + s_out:
+        q.wait_event(e0)
     for _ in range(steps):
         step()
-    s_out.wait_event(gemm_done[-1])
-    for q in (s_in, stream):
+    for q in s_in + s_out:
         j = torch.cuda.Event()
         j.record(q)
-        s_out.wait_event(j)
-    e1.record(s_out)
+        stream.wait_event(j)
+    e1.record(stream)
     torch.cuda.synchronize()
     control.barrier()
     secs = e0.elapsed_time(e1) / 1e3
@@ -447,7 +463,7 @@ def run_e2e(work, launch, stream, args, control, dev):
     _, _, v = aggregate(control, flops, secs)
     return {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(1e3 * secs / steps, 3),
-            "pipeline": "H2D / GEMM / D2H on three streams, overlapped across workloads"}
+            "pipeline": "H2D / GEMM / D2H overlapped across workloads; each copy split over %d streams" % nsplit}
 
 
 def stored_traffic(workload):
@@ -520,6 +536,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-split", type=int, default=1, help="copy streams per direction in the e2e leg")
     ap.add_argument("--cpu-rows", type=int, default=1536)
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
