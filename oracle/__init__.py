@@ -47,6 +47,10 @@ def lib():
         L.sgo_gemm_points.argtypes = [ctypes.c_int, i64, i64, i64, vp, vp, vp, vp, i64, vp, vp, vp, vp]
         L.sgo_num_threads.restype = ctypes.c_int
         L.sgo_num_threads.argtypes = []
+        L.sgo_e4m3_rne_sat.restype = ctypes.c_uint8
+        L.sgo_e4m3_rne_sat.argtypes = [ctypes.c_double]
+        L.sgo_quantize.restype = ctypes.c_int
+        L.sgo_quantize.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -139,3 +143,36 @@ def bits_to_f64(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) -> float64 values, via the oracle's own decoder rule."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def e4m3_rne_sat(x) -> np.ndarray:
+    """Nearest e4m3fn codes (ties to even, saturated to +-448) of binary64 values."""
+    L = lib()
+    v = np.asarray(x, dtype=np.float64)
+    return np.array([L.sgo_e4m3_rne_sat(float(t)) for t in v.ravel()], dtype=np.uint8).reshape(v.shape)
+
+
+def quantize(mode, X):
+    """Quantise X [R, C] (float32, or uint16 bf16 bits) in `mode` ("ptpc",
+    "blockscale" 1x128, "mxfp8" 1x32) into (codes uint8 [R, C], scales) with the
+    scales in the GEMM's A-side layout: ptpc float32 [R]; blockscale float32
+    [C/128, R]; mxfp8 uint8 e8m0 [C/32, R]."""
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    X = np.ascontiguousarray(X)
+    bf16 = X.dtype == np.uint16
+    if not bf16:
+        X = X.astype(np.float32, copy=False)
+    R, C = X.shape
+    Q = np.empty((R, C), dtype=np.uint8)
+    if m == 1:
+        S = np.empty(R, dtype=np.float32)
+    elif m == 2:
+        S = np.empty((C // 128, R), dtype=np.float32)
+    elif m == 3:
+        S = np.empty((C // 32, R), dtype=np.uint8)
+    else:
+        raise ValueError("quantize: mode must be ptpc, blockscale or mxfp8")
+    rc = lib().sgo_quantize(m, int(bf16), R, C, _ptr(X), _ptr(Q), _ptr(S))
+    if rc != 0:
+        raise ValueError("oracle quantize rejected its arguments (rc=%d)" % rc)
+    return Q, S

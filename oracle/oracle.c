@@ -256,3 +256,108 @@ int sgo_num_threads(void) {
     return 1;
 #endif
 }
+
+/* ---- quantisation to e4m3 + scales (the step before the GEMM) -----------------
+ *
+ * ROCm/mori PR 809, "Using it": a_fp8, a_scale = quantize_per_token(x) -- the
+ * activations are quantised per row (per token) before the ptpc GEMM; the
+ * blockscale and mxfp8 modes take per-block scales (the same PR, "Not done yet":
+ * the blockscale / mxfp8 A scale is K-block major).  Definition used here, for
+ * a row segment (whole row, 128 or 32 elements) with amax = max |x|:
+ *   ptpc / blockscale  s = fp32(amax / 448) (s = 1 if amax == 0);
+ *                      q = e4m3_rne_satfinite(fp32(x / s))
+ *   mxfp8              e = the least integer with amax <= 448 * 2^e (e = 0 if
+ *                      amax == 0); code = clamp(e + 127, 0, 254); s = 2^(code-127);
+ *                      q = e4m3_rne_satfinite(fp32(x / s))
+ * fp32(.) is one IEEE round-to-nearest-even fp32 operation; e4m3_rne_satfinite
+ * rounds to the nearest e4m3fn value (ties to even) and clamps to +-448.       */
+
+/* Nearest e4m3fn code to the binary64 value v, ties to even, saturated to
+ * +-448.  NaN -> 0x7F.                                                         */
+uint8_t sgo_e4m3_rne_sat(double v) {
+    if (v != v) return 0x7F;
+    uint8_t sign = (uint8_t)(signbit(v) ? 0x80 : 0x00);
+    double a = fabs(v);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    if (a == 0.0) return sign;
+    int ex;
+    frexp(a, &ex);              /* a in [2^(ex-1), 2^ex) */
+    int E = ex - 1;             /* unbiased exponent of a */
+    if (E < -6) E = -6;         /* subnormal range shares the 2^-9 quantum */
+    double q = ldexp(1.0, E - 3);
+    double n = a / q;           /* exact: q is a power of two */
+    double fl = floor(n);
+    double rem = n - fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    double r = fl * q;          /* exact: fl <= 16 */
+    if (r >= 448.0) return (uint8_t)(sign | 0x7E);
+    if (r == 0.0) return sign;
+    int ex2;
+    frexp(r, &ex2);
+    int E2 = ex2 - 1;
+    if (E2 < -6) { /* subnormal: r = f * 2^-9, f in 1..7 */
+        int f = (int)(r / ldexp(1.0, -9));
+        return (uint8_t)(sign | f);
+    }
+    int f = (int)((r / ldexp(1.0, E2) - 1.0) * 8.0);
+    return (uint8_t)(sign | ((E2 + 7) << 3) | f);
+}
+
+/* Least integer e with amax <= 448 * 2^e (amax > 0), by exact comparison. */
+static int sgo_mx_exponent(double amax) {
+    int e = ilogb(amax) - 8;
+    while (448.0 * ldexp(1.0, e) < amax) ++e;
+    while (448.0 * ldexp(1.0, e - 1) >= amax) --e;
+    return e;
+}
+
+/* Quantise X [R][C] (x_is_bf16: uint16 bf16 bits, else float32) in `mode`
+ * (1 ptpc, 2 blockscale 1x128, 3 mxfp8 1x32) into Q [R][C] e4m3 codes and
+ * scales (ptpc float[R]; blockscale float[C/128][R]; mxfp8 uint8[C/32][R]).
+ * Returns 0, or -1 on a bad argument.                                        */
+int sgo_quantize(int mode, int x_is_bf16, int64_t R, int64_t C, const void* X, uint8_t* Q,
+                 void* scale) {
+    int64_t blk;
+    if (mode == SGO_MODE_PTPC) blk = C;
+    else if (mode == SGO_MODE_BLOCKSCALE) blk = 128;
+    else if (mode == SGO_MODE_MXFP8) blk = 32;
+    else return -1;
+    if (R < 0 || C < 0 || (blk > 0 && C % blk != 0)) return -1;
+    if (R == 0 || C == 0) return 0;
+    int64_t nblk = C / blk;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t j = 0; j < nblk; ++j) {
+            float amax = 0.0f;
+            for (int64_t k = j * blk; k < (j + 1) * blk; ++k) {
+                float x = x_is_bf16 ? (float)sgo_dec_bf16(((const uint16_t*)X)[r * C + k])
+                                    : ((const float*)X)[r * C + k];
+                float a = fabsf(x);
+                if (a > amax) amax = a;
+            }
+            float s;
+            if (mode == SGO_MODE_MXFP8) {
+                int e = amax > 0.0f ? sgo_mx_exponent((double)amax) : 0;
+                int code = e + 127;
+                if (code < 0) code = 0;
+                if (code > 254) code = 254;
+                ((uint8_t*)scale)[j * R + r] = (uint8_t)code;
+                s = (float)ldexp(1.0, code - 127);
+            } else {
+                volatile float num = amax, den = 448.0f;
+                s = amax > 0.0f ? num / den : 1.0f;
+                if (mode == SGO_MODE_PTPC)
+                    ((float*)scale)[r] = s;
+                else
+                    ((float*)scale)[j * R + r] = s;
+            }
+            for (int64_t k = j * blk; k < (j + 1) * blk; ++k) {
+                float x = x_is_bf16 ? (float)sgo_dec_bf16(((const uint16_t*)X)[r * C + k])
+                                    : ((const float*)X)[r * C + k];
+                volatile float y = x / s; /* one fp32 IEEE division */
+                Q[r * C + k] = sgo_e4m3_rne_sat((double)y);
+            }
+        }
+    }
+    return 0;
+}

@@ -16,6 +16,7 @@ import pytest
 import oracle
 import test_oracle_decoders as dec
 import test_oracle_gemm as gem
+import test_oracle_quantize as qnt
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -31,6 +32,9 @@ MUTANTS = {
     "mx_scale_index": ("s_b = sgo_dec_e8m0(((const uint8_t*)sb)[j * N + n]);", "s_b = sgo_dec_e8m0(((const uint8_t*)sb)[n]);"),
     "ties_away": ("if (rem > half || (rem == half && (n & 1))) n += 1;", "if (rem >= half) n += 1;"),
     "bf16_decode_shift": ("uint32_t bits = (uint32_t)h << 16;", "uint32_t bits = (uint32_t)h << 15;"),
+    "e4m3_ties_away": ("if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;", "if (rem >= 0.5) fl += 1.0;"),
+    "mx_exponent_off_by_one": ("    while (448.0 * ldexp(1.0, e - 1) >= amax) --e;\n    return e;", "    while (448.0 * ldexp(1.0, e - 1) >= amax) --e;\n    return e + 1;"),
+    "quant_scale_448": ("volatile float num = amax, den = 448.0f;", "volatile float num = amax, den = 480.0f;"),
 }
 
 
@@ -47,6 +51,10 @@ def _pins():
         yield (lambda f=fields: gem.test_worked_examples(f))
     for mode in ("ptpc", "blockscale", "mxfp8", "bf16"):
         yield (lambda m=mode: gem.test_float64_library_matmul(m))
+    yield qnt.test_e4m3_rounding_matches_torch_within_range
+    yield qnt.test_e4m3_ties_and_saturation
+    yield qnt.test_ptpc_quantisation_equals_the_input_generator_on_float32
+    yield qnt.test_mx_exponent_is_the_least_power_that_covers_amax
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -61,7 +69,7 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
         subprocess.run(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", so, c, "-lm"], check=True)
         real = oracle.lib()
         mut = ctypes.CDLL(so)
-        for fn in ("sgo_dec_e4m3", "sgo_dec_e8m0", "sgo_dec_bf16", "sgo_bf16_rne", "sgo_gemm_rows", "sgo_gemm_points", "sgo_num_threads"):
+        for fn in ("sgo_dec_e4m3", "sgo_dec_e8m0", "sgo_dec_bf16", "sgo_bf16_rne", "sgo_gemm_rows", "sgo_gemm_points", "sgo_num_threads", "sgo_e4m3_rne_sat", "sgo_quantize"):
             getattr(mut, fn).restype = getattr(real, fn).restype
             getattr(mut, fn).argtypes = getattr(real, fn).argtypes
         monkeypatch.setattr(oracle, "_lib", mut)
