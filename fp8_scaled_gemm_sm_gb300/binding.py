@@ -35,7 +35,9 @@ SIGNATURES = {
     "scaled_gemm_debug_status": (_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "scaled_gemm_set_debug": (_int, [_vp, _i64, _i64]),
     "scaled_gemm_launch_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "scaled_gemm_quantize": (_int, [_int, _int, _vp, _i64, _i64, _vp, _vp, _vp]),
 }
+DTYPES = {"bf16": 0, "f32": 1}
 
 
 class ScaledGemmError(RuntimeError):
@@ -94,6 +96,37 @@ def scaled_gemm_launch_noalloc(A, B, a_scale, b_scale, C, M, N, K, stream=0):
         lib().scaled_gemm_launch_noalloc(A, B, a_scale, b_scale, C, int(M), int(N), int(K), stream or None),
         "scaled_gemm_launch_noalloc",
     )
+
+
+def scaled_gemm_quantize(mode, x_dtype, X, R, C, Q, scale, stream=0):
+    """Quantise X [R, C] (device pointer) to e4m3 codes Q and scales (see the C header)."""
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    dt = DTYPES[x_dtype] if isinstance(x_dtype, str) else int(x_dtype)
+    _check(lib().scaled_gemm_quantize(m, dt, X, int(R), int(C), Q, scale, stream or None), "scaled_gemm_quantize")
+
+
+def quantize(mode, x, stream=None):
+    """Quantise a CUDA tensor x [R, C] (bfloat16 or float32) for `mode`; returns
+    (codes uint8 [R, C], scales) with scales float32 [R] (ptpc), float32
+    [C/128, R] (blockscale) or uint8 [C/32, R] (mxfp8)."""
+    import torch
+
+    if x.dtype not in (torch.bfloat16, torch.float32) or x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("quantize: x must be a contiguous 2-D bfloat16 or float32 CUDA tensor")
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    if mode == "ptpc":
+        s = torch.empty(R, dtype=torch.float32, device=x.device)
+    elif mode == "blockscale":
+        s = torch.empty((C // 128, R), dtype=torch.float32, device=x.device)
+    elif mode == "mxfp8":
+        s = torch.empty((C // 32, R), dtype=torch.uint8, device=x.device)
+    else:
+        raise ValueError("quantize: mode must be ptpc, blockscale or mxfp8")
+    st = torch.cuda.current_stream(x.device).cuda_stream if stream is None else stream
+    scaled_gemm_quantize(mode, "bf16" if x.dtype == torch.bfloat16 else "f32", x.data_ptr(), R, C,
+                         q.data_ptr(), s.data_ptr(), st)
+    return q, s
 
 
 def scaled_gemm_destroy(h):

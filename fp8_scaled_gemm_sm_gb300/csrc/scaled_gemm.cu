@@ -290,4 +290,24 @@ sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, cons
   return r == SG_OK ? SG_OK : fail(r, "launch: kernel launch");
 }
 
+sg_status_t scaled_gemm_quantize(int mode, int x_dtype, const void* X, int64_t R, int64_t C, void* Q,
+                                 void* scale, sg_stream_t stream) {
+  if (mode != SG_MODE_PTPC && mode != SG_MODE_BLOCKSCALE && mode != SG_MODE_MXFP8)
+    return fail(SG_ERR_INVALID_ARG, "quantize: mode must be ptpc, blockscale or mxfp8");
+  if (x_dtype != SG_DTYPE_BF16 && x_dtype != SG_DTYPE_F32) return fail(SG_ERR_INVALID_ARG, "quantize: bad x_dtype");
+  if (R < 0 || C < 0) return fail(SG_ERR_INVALID_ARG, "quantize: negative size");
+  if (R > kMaxDim || C > sg::quantize_max_cols()) return fail(SG_ERR_UNSUPPORTED_SHAPE, "quantize: R >= 2^31 or C > 32768");
+  if (C % k_multiple(mode) != 0) return fail(SG_ERR_UNSUPPORTED_SHAPE, "quantize: C not a multiple of the mode's block");
+  if (R == 0 || C == 0) return SG_OK;
+  if (!X || !Q || !scale) return fail(SG_ERR_INVALID_ARG, "quantize: NULL pointer");
+  if (!aligned16(X) || !aligned16(Q) || !aligned16(scale)) return fail(SG_ERR_MISALIGNED, "quantize: pointer");
+  int dev = -1, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return fail(SG_ERR_CUDA, "quantize: device query");
+  const sg_status_t r = sg::quantize_launch(mode, x_dtype == SG_DTYPE_BF16, X, R, C, Q, scale, sms,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return r == SG_OK ? SG_OK : fail(r, "quantize: kernel launch");
+}
+
 }  // extern "C"

@@ -52,6 +52,10 @@ inline sg_status_t launch_status() {
   return SG_ERR_CUDA;
 }
 
+int64_t quantize_max_cols();
+sg_status_t quantize_launch(int mode, bool bf16, const void* X, int64_t R, int64_t C, void* Q,
+                            void* scale, int num_sms, cudaStream_t st);
+
 cudaError_t dense_prepare(int mode);
 sg_status_t dense_launch(const LaunchArgs& a);
 void dense_config(int mode, int64_t K, TileConfig* c);

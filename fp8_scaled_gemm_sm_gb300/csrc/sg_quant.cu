@@ -1,0 +1,197 @@
+// sg_quant.cu -- the step before the GEMM: quantise activations X [R][C] (bf16 or
+// fp32) to e4m3 codes plus scales in the layouts the GEMM kernels read.
+//
+// ROCm/mori PR 809, "Using it": a_fp8, a_scale = quantize_per_token(x) feeds the
+// ptpc GEMM; the same PR's "Not done yet" gives the blockscale / mxfp8 A scales
+// as K-block major.  For a row segment (the whole row for ptpc, 128 elements for
+// blockscale, 32 for mxfp8) with amax = max |x|:
+//   ptpc / blockscale  s = amax / 448 (one fp32 IEEE division; s = 1 if amax = 0)
+//   mxfp8              e = the least integer with amax <= 448 * 2^e (0 if amax = 0),
+//                      code = clamp(e + 127, 0, 254), s = 2^(code - 127)
+//   q = e4m3(x / s): one fp32 IEEE division, then round to nearest even with
+//   saturation to +-448 (cvt.rn.satfinite).
+//
+// One CTA of 256 threads per row (persistent over rows).  Thread t holds the
+// 8-element vectors t, t + 256, ... of its row in registers (16-byte loads), so
+// the row is read once; the amax of a 128-element block lives in 16 consecutive
+// lanes and that of a 32-element block in 4, reduced with warp shuffles; a row
+// amax (ptpc) is reduced across the CTA.  The kernel is bound by HBM: it reads
+// 2 (bf16) or 4 (fp32) bytes and writes 1 byte per element, plus the scales.
+#include <cuda.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "sg_common.cuh"
+#include "sg_internal.h"
+
+namespace sg {
+
+namespace {
+
+constexpr int kQThreads = 256;
+constexpr int kQMaxVecs = 16;  // vectors per thread: C <= 16 * 256 * 8 = 32768
+
+// Least integer e with amax <= 448 * 2^e, for finite amax > 0, by exact integer
+// comparison: amax = M * 2^q, 448 = 7 * 2^6, so e = t - 6 + q with t the least
+// integer such that 7 * 2^t >= M.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const uint32_t u = __float_as_uint(amax);
+  const uint32_t ef = (u >> 23) & 0xFFu;
+  const uint64_t M = ef ? ((u & 0x7FFFFFu) | 0x800000u) : (u & 0x7FFFFFu);
+  const int q = ef ? static_cast<int>(ef) - 150 : -149;
+  int t = 0;
+  if (M > 7) {
+    while ((7ull << t) < M) ++t;
+  } else {
+    while ((M << (1 - t)) <= 7) --t;
+  }
+  return t - 6 + q;
+}
+
+__device__ __forceinline__ float exp2_code(int code) {  // 2^(code - 127), code in [0, 254]
+  return code > 0 ? __uint_as_float(static_cast<uint32_t>(code) << 23) : __uint_as_float(0x00400000u);
+}
+
+template <bool BF16>
+__device__ __forceinline__ void load8(const void* X, int64_t elem, float (&f)[8]) {
+  if constexpr (BF16) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(X) + elem));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(X) + elem);
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+}
+
+// Eight codes of x / s, two per conversion (round to nearest even, saturated).
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  uint32_t w[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 y = make_float2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+    const uint32_t pair = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+    w[i >> 1] |= (pair & 0xFFFFu) << (16 * (i & 1));
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+template <int MODE, bool BF16, int VPT>
+__global__ void __launch_bounds__(kQThreads)
+    quantize_kernel(const void* __restrict__ X, uint8_t* __restrict__ Q, void* __restrict__ scale,
+                    int R, int C) {
+  __shared__ float red[kQThreads / 32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int nvec = C / 8;
+  for (int r = blockIdx.x; r < R; r += gridDim.x) {
+    const int64_t row = static_cast<int64_t>(r) * C;
+    float f[VPT][8];
+    float local = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = tid + i * kQThreads;
+      if (v < nvec) {
+        load8<BF16>(X, row + 8 * static_cast<int64_t>(v), f[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[i][j] = 0.f;
+      }
+    }
+    if constexpr (MODE == kModePtpc) {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) local = fmaxf(local, fabsf(f[i][j]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
+      if (lane == 0) red[tid >> 5] = local;
+      __syncthreads();
+      float amax = 0.f;
+#pragma unroll
+      for (int w = 0; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+      const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      if (tid == 0) static_cast<float*>(scale)[r] = s;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = tid + i * kQThreads;
+        if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s);
+      }
+      __syncthreads();  // red[] is reused by the next row
+    } else {
+      // a block is 16 (1x128) or 4 (1x32) consecutive vectors = lanes of one warp
+      constexpr int kLanes = MODE == kModeBlockscale ? 16 : 4;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[i][j]));
+#pragma unroll
+        for (int o = kLanes / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        const int v = tid + i * kQThreads;
+        const int blk = v / kLanes;
+        float s;
+        if constexpr (MODE == kModeBlockscale) {
+          s = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
+          if (v < nvec && (v % kLanes) == 0) static_cast<float*>(scale)[static_cast<int64_t>(blk) * R + r] = s;
+        } else {
+          int code = a > 0.f ? mx_exponent(a) + 127 : 127;
+          code = code < 0 ? 0 : (code > 254 ? 254 : code);
+          s = exp2_code(code);
+          if (v < nvec && (v % kLanes) == 0)
+            static_cast<uint8_t*>(scale)[static_cast<int64_t>(blk) * R + r] = static_cast<uint8_t>(code);
+        }
+        if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s);
+      }
+    }
+  }
+}
+
+template <int MODE, bool BF16, int VPT>
+sg_status_t launch_q(const void* X, uint8_t* Q, void* S, int R, int C, int grid, cudaStream_t st) {
+  quantize_kernel<MODE, BF16, VPT><<<grid, kQThreads, 0, st>>>(X, Q, S, R, C);
+  return launch_status();
+}
+
+template <int MODE, bool BF16>
+sg_status_t launch_q_vpt(const void* X, uint8_t* Q, void* S, int R, int C, int grid, cudaStream_t st) {
+  const int vecs = (C / 8 + kQThreads - 1) / kQThreads;
+  if (vecs <= 1) return launch_q<MODE, BF16, 1>(X, Q, S, R, C, grid, st);
+  if (vecs <= 2) return launch_q<MODE, BF16, 2>(X, Q, S, R, C, grid, st);
+  if (vecs <= 4) return launch_q<MODE, BF16, 4>(X, Q, S, R, C, grid, st);
+  if (vecs <= 8) return launch_q<MODE, BF16, 8>(X, Q, S, R, C, grid, st);
+  return launch_q<MODE, BF16, 16>(X, Q, S, R, C, grid, st);
+}
+
+template <int MODE>
+sg_status_t launch_q_mode(bool bf16, const void* X, uint8_t* Q, void* S, int R, int C, int grid,
+                          cudaStream_t st) {
+  return bf16 ? launch_q_vpt<MODE, true>(X, Q, S, R, C, grid, st)
+              : launch_q_vpt<MODE, false>(X, Q, S, R, C, grid, st);
+}
+
+}  // namespace
+
+int64_t quantize_max_cols() { return static_cast<int64_t>(kQMaxVecs) * kQThreads * 8; }
+
+sg_status_t quantize_launch(int mode, bool bf16, const void* X, int64_t R, int64_t C, void* Q,
+                            void* scale, int num_sms, cudaStream_t st) {
+  const int r = static_cast<int>(R), c = static_cast<int>(C);
+  const int64_t g = R < static_cast<int64_t>(num_sms) * 8 ? R : static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(g);
+  uint8_t* q = static_cast<uint8_t*>(Q);
+  switch (mode) {
+    case kModePtpc: return launch_q_mode<kModePtpc>(bf16, X, q, scale, r, c, grid, st);
+    case kModeBlockscale: return launch_q_mode<kModeBlockscale>(bf16, X, q, scale, r, c, grid, st);
+    case kModeMxfp8: return launch_q_mode<kModeMxfp8>(bf16, X, q, scale, r, c, grid, st);
+  }
+  return SG_ERR_INVALID_ARG;
+}
+
+}  // namespace sg

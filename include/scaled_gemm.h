@@ -125,6 +125,27 @@ sg_status_t scaled_gemm_debug_status(sg_handle_t h, sg_stream_t stream, int32_t*
  * expires.  Not for production use.                                              */
 sg_status_t scaled_gemm_set_debug(sg_handle_t h, int64_t timeout_ns, int64_t skip_kstep);
 
+/* Element types of the activations given to scaled_gemm_quantize. */
+typedef enum { SG_DTYPE_BF16 = 0, SG_DTYPE_F32 = 1 } sg_dtype_t;
+
+/* The step before the GEMM: quantise X [R][C] (row-major; bf16 or fp32 per
+ * x_dtype; finite values) to e4m3 codes Q [R][C] and scales in the A-side layout
+ * of `mode`:
+ *   SG_MODE_PTPC        scale float[R]         one per row (per token)
+ *   SG_MODE_BLOCKSCALE  scale float[C/128][R]  one per 1 x 128 block, K-block major
+ *   SG_MODE_MXFP8       scale uint8[C/32][R]   e8m0, one per 32 elements, K-block major
+ * For a row segment with amax = max |x|: ptpc / blockscale s = amax / 448 (one fp32
+ * IEEE division; 1 if amax == 0); mxfp8 e = the least integer with amax <= 448 * 2^e
+ * (0 if amax == 0), code = clamp(e + 127, 0, 254), s = 2^(code - 127).  Every code is
+ * q = e4m3(x / s): one fp32 IEEE division, then round to nearest even, saturated to
+ * +-448.  Shape rules: C % 16 == 0 (ptpc), C % 128 (blockscale), C % 32 (mxfp8),
+ * C <= 32768; pointers 16-byte aligned, device memory, caller-owned.  Asynchronous
+ * on `stream`.  Cited: ROCm/mori PR 809, "Using it" (a_fp8, a_scale =
+ * quantize_per_token(x) before the GEMM) and "Not done yet" (blockscale / mxfp8 A
+ * scales are K-block major).                                                    */
+sg_status_t scaled_gemm_quantize(int mode, int x_dtype, const void* X, int64_t R, int64_t C, void* Q,
+                                 void* scale, sg_stream_t stream);
+
 /* ptpc GEMM for callers that cannot allocate device memory.  (The paper has no
  * counterpart: this entry point belongs to this library's interface only.)
  *

@@ -87,3 +87,16 @@ def test_noalloc_rejects_bad_arguments_on_the_host(lib):
     assert f(None, None, None, None, None, 0, 256, 256, None) == 0    # empty: nothing to do
     assert f(None, None, None, None, None, 16, 256, 256, None) == 1   # NULL operands
     assert f(16, 32, 48, 64, 8, 16, 256, 256, None) == 3              # C misaligned
+
+
+def test_quantize_rejects_bad_arguments_on_the_host(lib):
+    f = binding.lib().scaled_gemm_quantize
+    assert f(0, 0, None, 4, 128, None, None, None) == 1        # bf16 mode is not a quantisation mode
+    assert f(1, 7, None, 4, 128, None, None, None) == 1        # bad dtype
+    assert f(1, 0, None, 4, 24, None, None, None) == 2         # C % 16
+    assert f(2, 0, None, 4, 64, None, None, None) == 2         # C % 128
+    assert f(3, 0, None, 4, 48, None, None, None) == 2         # C % 32
+    assert f(1, 0, None, 4, 65536, None, None, None) == 2      # C too large
+    assert f(1, 0, None, 0, 128, None, None, None) == 0        # nothing to do
+    assert f(1, 0, None, 4, 128, None, None, None) == 1        # NULL pointers
+    assert f(1, 0, 16, 4, 128, 8, 32, None) == 3               # misaligned
