@@ -290,8 +290,13 @@ def run_gpu(args, control, rank, local):
             "tile": "%dx%d" % (d["cfg"]["bm"], d["cfg"]["bn"]), "grid": d["cfg"]["grid"],
         }
 
-    # dominant kernel: the workload with the largest device time in the step
-    dom = max(per, key=lambda k: per[k]["us"])
+    # dominant kernel: the one with the largest share of the step's device time
+    # (the ptpc pair kernel); its launch with the most work is reported
+    share = {}
+    for k, v in per.items():
+        share[v["mode"]] = share.get(v["mode"], 0.0) + v["us"]
+    dom_mode = max(share, key=share.get)
+    dom = max((k for k in per if per[k]["mode"] == dom_mode), key=lambda k: per[k]["M"] * per[k]["N"] * per[k]["K"])
     pc = per[dom]
     dom_flops = 2.0 * pc["M"] * pc["N"] * pc["K"]
     achieved = dom_flops / (pc["us"] * 1e-6) / 1e12
@@ -329,6 +334,8 @@ def run_gpu(args, control, rank, local):
         code, _ = binding.scaled_gemm_debug_status(d["h"], sraw)
         status_bad += code != 0
 
+    quant = None if args.no_quant else run_quantize(binding, dev, stream, hbm)
+
     # end to end through the C ABI with host buffers: H2D inputs, GEMM, D2H C
     e2e = None if args.no_e2e else run_e2e(work, launch, stream, args, control, dev)
 
@@ -356,6 +363,7 @@ def run_gpu(args, control, rank, local):
             % (sum(d["A"].numel() * d["A"].element_size() + d["B"].numel() * d["B"].element_size() for d in work) / 1e9),
         },
         "roofline": roofline,
+        "quantize": quant,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
@@ -368,6 +376,41 @@ def run_gpu(args, control, rank, local):
                   "bf16_tflops_sustained": bf16_peak, "hbm_gbs": hbm},
     }
     return line
+
+
+def run_quantize(binding, dev, stream, hbm, R=32768, C=7168, iters=20):
+    """The quantisation step before the GEMM, timed on its own (not part of the
+    suite value): the largest activation of the workloads, R x C bf16, in every
+    mode.  HBM-bound: algorithmic bytes = 2RC read + RC written + the scales."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    x = torch.randn(R, C, generator=g, device=dev, dtype=torch.float32).bfloat16()
+    out = {}
+    sraw = stream.cuda_stream
+    for mode in ("ptpc", "blockscale", "mxfp8"):
+        q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+        if mode == "ptpc":
+            sc = torch.empty(R, dtype=torch.float32, device=dev)
+        elif mode == "blockscale":
+            sc = torch.empty((C // 128, R), dtype=torch.float32, device=dev)
+        else:
+            sc = torch.empty((C // 32, R), dtype=torch.uint8, device=dev)
+        f = lambda: binding.scaled_gemm_quantize(mode, "bf16", x.data_ptr(), R, C, q.data_ptr(), sc.data_ptr(), sraw)  # noqa: E731
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                f()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(iters):
+                f()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / iters
+        byts = 3.0 * R * C + sc.numel() * sc.element_size()
+        gbs = byts / (us * 1e-6) / 1e9
+        out[mode] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 3)}
+    out["workload"] = "%dx%d bf16 -> e4m3 + scales, %d launches per mode, inputs larger than L2" % (R, C, iters)
+    return out
 
 
 def run_e2e(work, launch, stream, args, control, dev):
@@ -541,6 +584,7 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--no-quant", action="store_true", help="skip the quantisation measurement (profiling runs)")
     ap.add_argument("--no-bad-check", action="store_true", help="skip the 20-launch check (profiling runs)")
     ap.add_argument("--only", default=None, choices=synth.SUITE, help="one workload (profiling runs)")
     ap.add_argument("--rows", type=int, default=None, help="override M of the workload(s) (profiling runs)")

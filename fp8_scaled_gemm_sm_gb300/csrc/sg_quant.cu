@@ -41,7 +41,9 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   const int q = ef ? static_cast<int>(ef) - 150 : -149;
   int t = 0;
   if (M > 7) {
-    while ((7ull << t) < M) ++t;
+    // M has b bits, so 7 * 2^(b-3) < 2^b and 7 * 2^(b-2) >= 2^b > M: t is b-3 or b-2
+    const int b = 32 - __clz(static_cast<uint32_t>(M));
+    t = (7ull << (b - 3)) >= M ? b - 3 : b - 2;
   } else {
     while ((M << (1 - t)) <= 7) --t;
   }
@@ -71,11 +73,15 @@ __device__ __forceinline__ void load8(const void* X, int64_t elem, float (&f)[8]
 }
 
 // Eight codes of x / s, two per conversion (round to nearest even, saturated).
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+// POW2: s is a power of two whose reciprocal is representable, so x * (1/s) is
+// the same correctly rounded value as x / s.
+template <bool POW2 = false>
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, float inv_s = 0.f) {
   uint32_t w[2] = {0, 0};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 y = make_float2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
+    const float2 y = POW2 ? make_float2(f[2 * i] * inv_s, f[2 * i + 1] * inv_s)
+                          : make_float2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
     const uint32_t pair = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
     w[i >> 1] |= (pair & 0xFFFFu) << (16 * (i & 1));
   }
@@ -136,18 +142,20 @@ __global__ void __launch_bounds__(kQThreads)
         for (int o = kLanes / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
         const int v = tid + i * kQThreads;
         const int blk = v / kLanes;
-        float s;
         if constexpr (MODE == kModeBlockscale) {
-          s = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
+          const float s = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
           if (v < nvec && (v % kLanes) == 0) static_cast<float*>(scale)[static_cast<int64_t>(blk) * R + r] = s;
+          if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s);
         } else {
           int code = a > 0.f ? mx_exponent(a) + 127 : 127;
           code = code < 0 ? 0 : (code > 254 ? 254 : code);
-          s = exp2_code(code);
           if (v < nvec && (v % kLanes) == 0)
             static_cast<uint8_t*>(scale)[static_cast<int64_t>(blk) * R + r] = static_cast<uint8_t>(code);
+          // 1/s = 2^(127 - code), code in [0, 254]: representable (normal or 2^-127)
+          if (v < nvec)
+            *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) =
+                quant8<true>(f[i], 0.f, exp2_code(254 - code));
         }
-        if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s);
       }
     }
   }
