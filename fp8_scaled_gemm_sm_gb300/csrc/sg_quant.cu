@@ -15,8 +15,13 @@
 // 8-element vectors t, t + 256, ... of its row in registers (16-byte loads), so
 // the row is read once; the amax of a 128-element block lives in 16 consecutive
 // lanes and that of a 32-element block in 4, reduced with warp shuffles; a row
-// amax (ptpc) is reduced across the CTA.  The kernel is bound by HBM: it reads
-// 2 (bf16) or 4 (fp32) bytes and writes 1 byte per element, plus the scales.
+// amax (ptpc) is reduced across the CTA.  While a row is processed, the raw
+// vectors of the CTA's next row are already being loaded (where they fit in 32
+// registers a thread), so loads stay in flight through the arithmetic.  The
+// algorithmic traffic is 2 (bf16) or 4 (fp32) bytes read and 1 byte written per
+// element, plus the scales; mxfp8 (a power-of-two scale: a multiply) runs near
+// that bound, ptpc and blockscale (an IEEE division per element) are partly
+// bound by instruction issue.
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -54,38 +59,72 @@ __device__ __forceinline__ float exp2_code(int code) {  // 2^(code - 127), code 
   return code > 0 ? __uint_as_float(static_cast<uint32_t>(code) << 23) : __uint_as_float(0x00400000u);
 }
 
+// The raw 16 (bf16) or 32 (fp32) bytes of one 8-element vector.
 template <bool BF16>
-__device__ __forceinline__ void load8(const void* X, int64_t elem, float (&f)[8]) {
+struct Raw8 {
+  uint4 w[BF16 ? 1 : 2];
+};
+
+template <bool BF16>
+__device__ __forceinline__ void load_raw8(const void* X, int64_t elem, Raw8<BF16>& raw) {
   if constexpr (BF16) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(X) + elem));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    raw.w[0] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(X) + elem));
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(X) + elem);
+    raw.w[0] = __ldg(p);
+    raw.w[1] = __ldg(p + 1);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ void unpack8(const Raw8<BF16>& raw, float (&f)[8]) {
+  if constexpr (BF16) {
+    const uint32_t w[4] = {raw.w[0].x, raw.w[0].y, raw.w[0].z, raw.w[0].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       f[2 * i] = __uint_as_float(w[i] << 16);
       f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
   } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(X) + elem);
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      f[4 * h + 0] = __uint_as_float(raw.w[h].x);
+      f[4 * h + 1] = __uint_as_float(raw.w[h].y);
+      f[4 * h + 2] = __uint_as_float(raw.w[h].z);
+      f[4 * h + 3] = __uint_as_float(raw.w[h].w);
+    }
   }
 }
 
-// Eight codes of x / s, two per conversion (round to nearest even, saturated).
-// POW2: s is a power of two whose reciprocal is representable, so x * (1/s) is
-// the same correctly rounded value as x / s.
-template <bool POW2 = false>
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, float inv_s = 0.f) {
+__device__ __forceinline__ uint2 cvt8(const float (&y)[8]) {
   uint32_t w[2] = {0, 0};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 y = POW2 ? make_float2(f[2 * i] * inv_s, f[2 * i + 1] * inv_s)
-                          : make_float2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
-    const uint32_t pair = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t pair = __nv_cvt_float2_to_fp8x2(make_float2(y[2 * i], y[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
     w[i >> 1] |= (pair & 0xFFFFu) << (16 * (i & 1));
   }
   return make_uint2(w[0], w[1]);
+}
+
+// Eight codes of x / s (round to nearest even, saturated), s a power of two
+// whose reciprocal inv_s is representable: x * inv_s is then the same correctly
+// rounded value as x / s.
+__device__ __forceinline__ uint2 quant8_pow2(const float (&f)[8], float inv_s) {
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = f[i] * inv_s;
+  return cvt8(y);
+}
+
+// Eight codes of x / s: one IEEE fp32 division each, then e4m3.  (A reciprocal
+// multiply with a check for quotients near an e4m3 rounding midpoint was timed
+// as well: the check costs as many instructions as the division, and the
+// kernel is issue-bound there.)
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(f[i], s);
+  return cvt8(y);
 }
 
 template <int MODE, bool BF16, int VPT>
@@ -96,20 +135,45 @@ __global__ void __launch_bounds__(kQThreads)
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int nvec = C / 8;
+  // The next row's raw vectors are loaded while the current row is processed,
+  // where they fit in 32 registers; otherwise each row is loaded when it starts.
+  constexpr bool kPrefetch = VPT * (BF16 ? 4 : 8) <= 32;
+  auto fetch = [&](Raw8<BF16> (&dst)[VPT], int rr) {
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int v = tid + i * kQThreads;
+      if (v < nvec && rr < R) load_raw8<BF16>(X, static_cast<int64_t>(rr) * C + 8 * static_cast<int64_t>(v), dst[i]);
+    }
+  };
+  Raw8<BF16> next[kPrefetch ? VPT : 1];
+  if constexpr (kPrefetch) fetch(next, blockIdx.x);
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
     const int64_t row = static_cast<int64_t>(r) * C;
     float f[VPT][8];
     float local = 0.f;
+    if constexpr (kPrefetch) {
+      Raw8<BF16> raw[VPT];
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int v = tid + i * kQThreads;
-      if (v < nvec) {
-        load8<BF16>(X, row + 8 * static_cast<int64_t>(v), f[i]);
-      } else {
+      for (int i = 0; i < VPT; ++i) raw[i] = next[i];
+      fetch(next, r + gridDim.x);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[i][j] = 0.f;
+      for (int i = 0; i < VPT; ++i) unpack8<BF16>(raw[i], f[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = tid + i * kQThreads;
+        Raw8<BF16> raw;
+        if (v < nvec) load_raw8<BF16>(X, row + 8 * static_cast<int64_t>(v), raw);
+        unpack8<BF16>(raw, f[i]);
       }
     }
+    // vectors past the row end (the last pass when C / 8 is not a multiple of
+    // the block size) hold zeros
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+      if (tid + i * kQThreads >= nvec)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[i][j] = 0.f;
     if constexpr (MODE == kModePtpc) {
 #pragma unroll
       for (int i = 0; i < VPT; ++i)
@@ -145,7 +209,9 @@ __global__ void __launch_bounds__(kQThreads)
         if constexpr (MODE == kModeBlockscale) {
           const float s = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
           if (v < nvec && (v % kLanes) == 0) static_cast<float*>(scale)[static_cast<int64_t>(blk) * R + r] = s;
-          if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s);
+          if (v < nvec)
+            *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) =
+                quant8(f[i], s);
         } else {
           int code = a > 0.f ? mx_exponent(a) + 127 : 127;
           code = code < 0 ? 0 : (code > 254 ? 254 : code);
@@ -154,7 +220,7 @@ __global__ void __launch_bounds__(kQThreads)
           // 1/s = 2^(127 - code), code in [0, 254]: representable (normal or 2^-127)
           if (v < nvec)
             *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) =
-                quant8<true>(f[i], 0.f, exp2_code(254 - code));
+                quant8_pow2(f[i], exp2_code(254 - code));
         }
       }
     }

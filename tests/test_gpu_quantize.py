@@ -55,6 +55,48 @@ def test_quantize_bit_exact(lib, mode, dtype, R, C):
     assert np.array_equal(s.view(np.uint8), s_ref.view(np.uint8))
 
 
+def _near_ties(R, C, seed):
+    # Every 32-column group opens with the row's amax, so every block of every
+    # mode has scale s = fp32(amax / 448); the other entries are fp32(m * s)
+    # moved by -6..6 ulps, m an e4m3 rounding midpoint (normal, subnormal or
+    # the saturation point 464), or values whose quotient lies in the e4m3
+    # subnormal band.  The quotients land on and beside the midpoints, where
+    # the rounded fp32 quotient decides the code.
+    rng = np.random.default_rng(seed)
+    X = np.empty((R, C), np.float32)
+    for r in range(R):
+        amax = np.float32(np.exp2(rng.uniform(-60, 60)) * rng.uniform(1, 2))
+        s = np.float32(amax / np.float32(448.0))
+        e = rng.integers(-10, 9, C)
+        j = rng.integers(0, 8, C)
+        m = np.where(e >= -6, (1 + (2 * j + 1) / 16.0) * np.exp2(e), (2 * j + 1) * 2.0 ** -10)
+        m[rng.random(C) < 0.05] = 464.0
+        band = rng.random(C) < 0.1
+        m[band] = np.exp2(rng.uniform(-11, -6, band.sum()))
+        x = (m.astype(np.float32) * s).astype(np.float32)
+        x = (x.view(np.int32) + rng.integers(-6, 7, C).astype(np.int32)).view(np.float32)
+        x = np.minimum(x, amax) * np.where(rng.random(C) < 0.5, -1, 1).astype(np.float32)
+        x[::32] = amax
+        X[r] = x
+    return X
+
+
+@pytest.mark.parametrize("mode", ["ptpc", "blockscale", "mxfp8"])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_quantize_near_rounding_midpoints(lib, mode, bf16):
+    X = _near_ties(64, 1024, 11 + bf16)
+    x = torch.from_numpy(X)
+    if bf16:
+        x = x.bfloat16()  # rounding to bf16 keeps the quotients near the midpoints of a coarser grid
+    q_ref, s_ref = oracle.quantize(mode, _host(x))
+    q, s = lib.quantize(mode, x.cuda())
+    torch.cuda.synchronize()
+    q, s = q.cpu().numpy(), s.cpu().numpy()
+    bad = np.argwhere(q != q_ref)
+    assert bad.size == 0, [(tuple(i), hex(q[tuple(i)]), hex(q_ref[tuple(i)])) for i in bad[:5]]
+    assert np.array_equal(s.view(np.uint8), s_ref.view(np.uint8))
+
+
 def test_quantize_full_size_sampled_rows(lib):
     # the largest activation of the workloads, 32768 x 7168 bf16, every mode;
     # rows are independent, so the oracle checks a sample of them
