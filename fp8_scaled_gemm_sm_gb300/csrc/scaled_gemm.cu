@@ -21,6 +21,7 @@ struct sg_gemm {
   int device;
   int num_sms;
   int* status;  // device: [code, where, 0, 0]
+  void* workspace;  // device; mxfp8: the scale records of one launch (else NULL)
   uint64_t timeout_ns;
   int32_t skip_kstep;
 };
@@ -154,16 +155,21 @@ sg_status_t scaled_gemm_create(sg_handle_t* out, int mode, int64_t N, int64_t K,
     case SG_MODE_BLOCKSCALE: e = sg::blockscale_prepare(); break;
   }
   int* status = nullptr;
+  void* workspace = nullptr;
   if (e == cudaSuccess) e = cudaMalloc(&status, 16);
   if (e == cudaSuccess) e = cudaMemset(status, 0, 16);
+  const size_t ws_bytes = mode == SG_MODE_MXFP8 ? sg::mxfp8_workspace_bytes(M_max, N, K) : 0;
+  if (e == cudaSuccess && ws_bytes > 0) e = cudaMalloc(&workspace, ws_bytes);
   if (prev >= 0 && prev != dev) cudaSetDevice(prev);
   if (e != cudaSuccess) {
     if (status) cudaFree(status);
-    return fail(SG_ERR_CUDA, "create: kernel attributes / status word");
+    if (workspace) cudaFree(workspace);
+    return fail(SG_ERR_CUDA, "create: kernel attributes / status word / workspace");
   }
   sg_gemm* h = new (std::nothrow) sg_gemm;
   if (!h) {
     cudaFree(status);
+    if (workspace) cudaFree(workspace);
     return fail(SG_ERR_CUDA, "create: out of host memory");
   }
   h->mode = mode;
@@ -173,6 +179,7 @@ sg_status_t scaled_gemm_create(sg_handle_t* out, int mode, int64_t N, int64_t K,
   h->device = dev;
   h->num_sms = sms;
   h->status = status;
+  h->workspace = workspace;
   h->timeout_ns = kDefaultTimeoutNs;
   h->skip_kstep = -1;
   *out = h;
@@ -185,6 +192,10 @@ sg_status_t scaled_gemm_destroy(sg_handle_t h) {
   cudaGetDevice(&prev);
   if (prev != h->device) cudaSetDevice(h->device);
   cudaError_t e = cudaFree(h->status);
+  if (h->workspace) {
+    const cudaError_t e2 = cudaFree(h->workspace);
+    if (e == cudaSuccess) e = e2;
+  }
   if (prev >= 0 && prev != h->device) cudaSetDevice(prev);
   delete h;
   return e == cudaSuccess ? SG_OK : SG_ERR_CUDA;
@@ -203,9 +214,10 @@ sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int
   if (bn) *bn = c.bn;
   if (bk) *bk = c.bk;
   if (stages) *stages = c.stages;
-  if (grid) {
-    const int64_t tiles = ((h->M_max + c.bm - 1) / c.bm) * ((h->N + c.bn - 1) / c.bn);
-    *grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+  if (grid) {  // the launch's persistent CTAs: whole clusters, at most one CTA per SM
+    const int64_t groups = ((h->M_max + c.rows_per_group - 1) / c.rows_per_group) * ((h->N + c.bn - 1) / c.bn);
+    const int64_t max_groups = h->num_sms / c.cluster;
+    *grid = static_cast<int>((groups < max_groups ? groups : max_groups) * c.cluster);
   }
   return SG_OK;
 }
@@ -250,7 +262,6 @@ sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, cons
   if (!scaled && (a_scale || b_scale)) return fail(SG_ERR_INVALID_ARG, "launch: bf16 takes no scales");
   if (!aligned16(A) || !aligned16(B)) return fail(SG_ERR_MISALIGNED, "launch: A or B");
   if (scaled && (!aligned16(a_scale) || !aligned16(b_scale))) return fail(SG_ERR_MISALIGNED, "launch: scales");
-  if (h->mode == SG_MODE_MXFP8 && M % 16 != 0) return fail(SG_ERR_UNSUPPORTED_SHAPE, "launch: mxfp8 needs M % 16 == 0");
   // C must not overlap an operand (the kernel streams C while it still reads them).
   const int64_t el = h->mode == SG_MODE_BF16 ? 2 : 1;
   auto overlap = [](const void* p, int64_t pb, const void* q, int64_t qb) {
@@ -280,6 +291,7 @@ sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, cons
   a.status = h->status;
   a.timeout_ns = h->timeout_ns;
   a.skip_kstep = h->skip_kstep;
+  a.workspace = h->workspace;
   sg_status_t r = SG_ERR_INVALID_ARG;
   switch (h->mode) {
     case SG_MODE_BF16:

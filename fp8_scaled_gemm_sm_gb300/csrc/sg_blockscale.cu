@@ -330,6 +330,8 @@ void blockscale_config(TileConfig* c) {
   c->bn = kBsBN;
   c->bk = 128;
   c->stages = kBsStages;
+  c->cluster = 1;
+  c->rows_per_group = kBM;
 }
 
 }  // namespace sg

@@ -537,6 +537,7 @@ struct DenseKernel {
   static constexpr bool kPair = false;
   static constexpr int kThreads = 64 + 32 * EPI_WARPS;
   static constexpr int kCluster = CLUSTER;
+  static constexpr int kStages = STAGES;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
   }
@@ -548,6 +549,7 @@ struct PairKernel {
   static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX>;
   static constexpr int kThreads = 64 + 32 * EPI_WARPS;
   static constexpr int kCluster = 2;
+  static constexpr int kStages = STAGES;
   static constexpr int kBoxW = 32;
   static constexpr bool kPair = true;
   static cudaError_t prepare() {
@@ -649,7 +651,9 @@ void dense_config(int mode, int64_t K, TileConfig* c) {
   c->bm = kBM;
   c->bn = kDenseBN;
   c->bk = dense_bk(mode);
-  c->stages = short_k(mode, K) ? 3 : 4;
+  c->stages = short_k(mode, K) ? ShortK<kModePtpc>::kStages : LongK<kModePtpc>::kStages;
+  c->cluster = 2;  // both paths: pairs (pair MMA for long K, shared B for short K)
+  c->rows_per_group = 2 * kBM;
 }
 
 }  // namespace sg

@@ -24,6 +24,7 @@ struct LaunchArgs {
   int* status;          // device status word of the plan
   uint64_t timeout_ns;  // per-wait limit
   int32_t skip_kstep;   // watchdog tests: -1 = off
+  void* workspace;      // the plan's device workspace (mxfp8: scale records), or NULL
 };
 
 // Mode numbers as the launchers take them (equal to sg_mode_t).
@@ -32,6 +33,8 @@ constexpr int kModePtpcHost = SG_MODE_PTPC;
 
 struct TileConfig {
   int bm, bn, bk, stages;
+  int cluster;         // CTAs per cluster
+  int rows_per_group;  // output rows one cluster covers per tile (N block) it takes
 };
 
 // Encode a 2D tiled TMA descriptor (inner dimension first).  Returns false if
@@ -61,6 +64,7 @@ sg_status_t dense_launch(const LaunchArgs& a);
 void dense_config(int mode, int64_t K, TileConfig* c);
 
 cudaError_t mxfp8_prepare();
+size_t mxfp8_workspace_bytes(int64_t M_max, int64_t N, int64_t K);  // scale records
 sg_status_t mxfp8_launch(const LaunchArgs& a);
 void mxfp8_config(TileConfig* c);
 

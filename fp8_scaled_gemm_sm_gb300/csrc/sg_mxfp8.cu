@@ -5,28 +5,46 @@
 // with e4m3 operands and one e8m0 scale per 32 consecutive K elements of every
 // row of A and of B (ROCm/mori PR 785, cost table and Scope: the "mxfp8" mode).
 // The scales are applied inside the tensor core by
-// tcgen05.mma.kind::mxf8f6f4.block_scale.scale_vec::1X, which reads them from
-// TMEM; nothing is rescaled in the epilogue.
+// tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X, which reads
+// them from TMEM; nothing is rescaled in the epilogue.
 //
-// Per CTA (one per SM, persistent over 128 x 224 output tiles; 224 divides the
-// 7168-wide weight exactly and leaves TMEM room for the scale factors next to
-// two 224-column accumulators):
-//   warp 0     TMA producer: A, B and the two raw scale boxes (sa rows
-//              [4 K-blocks][128 m], sb rows [4][224 n], K-block major as they
-//              sit in memory) into stage s; one full[s] barrier covers all four.
-//   warp 1     TMEM owner and MMA issuer.  Per stage: wait sf_ready[s], copy the
-//              stage's scale factors shared -> TMEM with two tcgen05.cp (128x128b
-//              for A, 128x256b for B's two 128-row chunks), then 4 block-scaled
-//              MMAs (K = 32 each, scale-factor id k selects the k-th byte of each
-//              32-bit scale word), commit empty[s].
-//   warp 2     scale-factor warp: wait full[s], regroup the raw bytes into the
-//              layout the MMA reads (in every 32-lane quarter, lane r column c
-//              holds the word for row 32 c + r of a 128-row chunk, each word the
-//              four K-block scales of that row), fence the async proxy, arrive
-//              sf_ready[s].  Its fence also orders its generic reads of the raw
-//              boxes before the TMA refill of stage s (deepseek-ai/DeepGEMM PR 453,
-//              Fix).
-//   warps 3-6  epilogue: TMEM -> bf16 -> shared memory -> TMA store.
+// Two kernels per launch:
+//
+// 1. mx_scale_records_kernel rearranges the scales, which arrive K-block major
+//    ([K/32][M] and [K/32][N] bytes, ROCm/mori PR 809, Not done yet), into
+//    512-byte records in the plan's workspace, one per 128-row chunk and
+//    128-element K step: byte 16 r + 4 c + k of a record is the scale of row
+//    32 c + r of the chunk for the step's K block k.  That is the shared-memory
+//    source tcgen05.cp.32x128b.warpx4 copies to TMEM (32 lanes x 16 bytes,
+//    repeated by the copy into all four lane quarters), where the MMA expects,
+//    in every 32-lane quarter, lane r column c to hold the four K-block scales
+//    of row 32 c + r.  Missing rows and K blocks are 0 (their A / B values are
+//    zero-filled by TMA).  It reads and writes (M + N) K / 32 bytes.
+//
+// 2. mxfp8_pair_kernel: two CTAs on neighbouring SMs (a cluster of 2) compute
+//    one 256 x 224 output tile with the pair MMA.  Each CTA stages its own 128
+//    rows of A and 112 of the tile's 224 rows of B, so per SM the shared memory
+//    written by TMA and read by the MMA per FLOP is that of a 128 x 448 tile; a
+//    single-CTA 128 x 224 tile was bound by that traffic (44 KB written and
+//    44 KB read per 470-cycle stage).  224 divides the 7168-wide weight exactly
+//    and leaves TMEM room for the scale factors next to two 224-column
+//    accumulators.  The scale records travel with the operands: per stage each
+//    CTA loads its A record and the tile's two B records by TMA, and all of it
+//    completes the even CTA's full[s].  (Regrouping the raw scales in a warp of
+//    each CTA instead put a per-stage cross-CTA release on the critical path and
+//    ran 2x slower.)
+//
+// Per CTA of the pair kernel, persistent over pair tiles (N block fastest):
+//   warp 0     TMA producer: A rows, B half and scale records into stage s.
+//   warp 1     TMEM owner (both CTAs) and, in the even CTA, MMA issuer.  Per
+//              stage: wait full[s]; copy both CTAs' scale records to TMEM with
+//              three tcgen05.cp.cta_group::2.32x128b.warpx4 (each CTA's copy
+//              reads its own shared memory): A's chunk and B's two 128-row
+//              chunks; 4 pair MMAs (K = 32 each; scale-factor id k selects the
+//              k-th byte of each 32-bit scale word); commit empty[s] of both CTAs.
+//   warps 2-9  epilogue, two warps per TMEM lane quarter (columns 0-127 and
+//              128-223): TMEM -> bf16 -> shared memory -> TMA store; the release
+//              of an accumulator arrives on the even CTA's tmem_empty.
 // Scale factors live in TMEM per stage (12 columns each), so a copy for stage s
 // never overwrites scales that an MMA issued for an earlier stage still reads:
 // the copy for a stage's next round is issued only after that stage's empty
@@ -41,84 +59,118 @@ namespace sg {
 
 namespace {
 
-constexpr int kMxBN = 224;
-constexpr int kMxStages = 4;
-constexpr int kMxEpiWarps = 4;
-constexpr int kMxThreads = 96 + 32 * kMxEpiWarps;
+constexpr int kMxBN = 224;                 // N of a pair tile (and of each CTA's accumulator)
+constexpr int kMxBHalf = kMxBN / 2;        // B rows each CTA stages
+constexpr int kMxStages = 5;
+constexpr int kMxEpiWarps = 8;
+constexpr int kMxThreads = 64 + 32 * kMxEpiWarps;
+constexpr int kRec = 512;                  // bytes of one scale record (32 rows x 16 B)
 
 struct MxLayout {
   static constexpr int kAStage = kBM * kRowBytes;        // 16 KB
-  static constexpr int kBStage = kMxBN * kRowBytes;      // 28 KB
-  static constexpr int kRawA = 4 * kBM;                  // [4][128] e8m0
-  static constexpr int kRawB = 4 * kMxBN;                // [4][224] e8m0
-  static constexpr int kSfA = 2048;                      // 128 lanes x 16 B
-  static constexpr int kSfB = 4096;                      // 128 lanes x 32 B
+  static constexpr int kBStage = kMxBHalf * kRowBytes;   // 14 KB
+  static constexpr int kSfA = kRec;                      // A's record
+  static constexpr int kSfB = 2 * kRec;                  // B's two records
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kMxStages * kAStage;
   static constexpr int kOffC = kOffB + kMxStages * kBStage;
-  static constexpr int kOffRawA = kOffC + kMxEpiWarps * 2 * kCBoxBytes;
-  static constexpr int kOffRawB = kOffRawA + kMxStages * kRawA;
-  static constexpr int kOffSfA = kOffRawB + kMxStages * kRawB;
+  static constexpr int kOffSfA = kOffC + kMxEpiWarps * 2 * kCBoxBytes;
   static constexpr int kOffSfB = kOffSfA + kMxStages * kSfA;
   static constexpr int kOffBar = kOffSfB + kMxStages * kSfB;
-  static constexpr int kNumBars = 3 * kMxStages + 5;
+  static constexpr int kNumBars = 2 * kMxStages + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 4 * kMxStages;
   static constexpr int kDynSmem = kBytes + 1024;
-  static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "alignment");
-  static_assert(kOffRawA % 128 == 0 && kOffRawB % 128 == 0 && kRawB % 128 == 0, "TMA alignment");
-  static_assert(kOffSfA % 128 == 0 && kOffSfB % 128 == 0, "scale chunk alignment");
+  static_assert(kOffB % 1024 == 0 && kBStage % 1024 == 0 && kOffC % 1024 == 0, "alignment");
+  static_assert(kOffSfA % 128 == 0 && kOffSfB % 128 == 0, "TMA / scale-record alignment");
+  static_assert(kDynSmem <= 232448, "shared memory");
 };
 
 // TMEM columns: accumulators at 0 and 256 (224 wide each); per-stage scale
-// factors in the gaps [224, 256) and [480, 512): A 4 columns, B 8 columns.
-__device__ __forceinline__ uint32_t sf_col_a(int s) { return s < 2 ? 224 + 12 * s : 480 + 12 * (s - 2); }
-__device__ __forceinline__ uint32_t sf_col_b(int s) { return sf_col_a(s) + 4; }
-
-// Scale factors go to TMEM with two copies per stage: tcgen05.cp.128x128b for A
-// (lane l, columns 0-3) and tcgen05.cp.128x256b for B (lane l, columns 0-7).
-// For a 128-row chunk the MMA takes, in every 32-lane quarter, lane r and column
-// c to hold the four K-block scales (bytes 0-3) of row 32 c + r of the chunk.
-// The shared-memory source is therefore the same 16 (A) or 32 (B) bytes for
-// lanes r, r+32, r+64, r+96, laid out in 8-row x 16-byte core matrices:
-// row l, 16-byte chunk j at (l / 8) * SBO + j * LBO + (l % 8) * 16.
-__device__ __forceinline__ uint64_t sf_desc_a(uint32_t addr) { return smem_desc(addr, 0, 128, 0); }
-__device__ __forceinline__ uint64_t sf_desc_b(uint32_t addr) { return smem_desc(addr, 128, 256, 0); }
-
-__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+// factors (A 4 columns, B 8) in the gaps [224, 256) and [480, 512).
+__device__ __forceinline__ uint32_t sf_col_a(int s) {
+  return s == 0 ? 224 : s == 1 ? 236 : s == 2 ? 480 : s == 3 ? 492 : 248;
 }
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+__device__ __forceinline__ uint32_t sf_col_b(int s) {
+  return s == 0 ? 228 : s == 1 ? 240 : s == 2 ? 484 : s == 3 ? 496 : 504;
+}
+static_assert(kMxStages <= 5, "TMEM has scale-factor room for 5 stages");
+
+// A 32-row x 16-byte record in shared memory as 8-row x 16-byte core matrices:
+// row r at (r / 8) * 128 + (r % 8) * 16 = 16 r.
+__device__ __forceinline__ uint64_t rec_desc(uint32_t addr) { return smem_desc(addr, 0, 128, 0); }
+
+__device__ __forceinline__ void tmem_cp_pair_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// The four 32-bit scale words lane r contributes for a 128-row chunk starting at
-// row0 of a raw K-block-major box ([4 K blocks][pitch] e8m0 bytes): word w holds
-// the 4 K-block scales of row row0 + 32 w + r (0 past rows_valid).
-__device__ __forceinline__ void sf_words(const uint8_t* raw, int pitch, int row0, int rows_valid, int lane,
-                                         uint32_t (&w)[4]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int row = row0 + 32 * q + lane;
-    uint32_t v = 0;
-    if (row < rows_valid) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v |= static_cast<uint32_t>(raw[k * pitch + row]) << (8 * k);
+// Records of the workspace.  A: record (mc, ks) at mc * k_steps + ks.  B: record
+// (nt, ks, j) at (nt * k_steps + ks) * 2 + j for 128-row chunk j of N tile nt.
+struct RecGeom {
+  int M, N, kblk, k_steps, m_chunks, n_tiles;
+  __host__ __device__ int64_t a_records() const { return static_cast<int64_t>(m_chunks) * k_steps; }
+  __host__ __device__ int64_t b_records() const { return static_cast<int64_t>(n_tiles) * k_steps * 2; }
+};
+
+// One thread per 32-bit word: the four K-block scales of one row.  Thread t of a
+// record handles row 32 c + r with r = t % 32, c = t / 32, so consecutive threads
+// read consecutive bytes of each K-block row of the source.
+__global__ void __launch_bounds__(256)
+    mx_scale_records_kernel(const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
+                            uint32_t* __restrict__ rec_a, uint32_t* __restrict__ rec_b, RecGeom g) {
+  const int64_t words_a = g.a_records() * 128;
+  const int64_t words_b = g.b_records() * 128;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < words_a + words_b;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const bool is_a = i < words_a;
+    const int64_t wi = is_a ? i : i - words_a;
+    const int64_t rec = wi >> 7;
+    const int t = static_cast<int>(wi & 127);
+    const int r = t & 31, c = t >> 5;
+    int row, ks, pitch;
+    const uint8_t* src;
+    bool valid;
+    if (is_a) {
+      const int mc = static_cast<int>(rec / g.k_steps);
+      ks = static_cast<int>(rec - static_cast<int64_t>(mc) * g.k_steps);
+      row = mc * kBM + 32 * c + r;
+      valid = row < g.M;
+      src = sa;
+      pitch = g.M;
+    } else {
+      const int j = static_cast<int>(rec & 1);
+      const int64_t q = rec >> 1;
+      const int nt = static_cast<int>(q / g.k_steps);
+      ks = static_cast<int>(q - static_cast<int64_t>(nt) * g.k_steps);
+      const int local = 128 * j + 32 * c + r;  // row within the 224-row tile
+      row = nt * kMxBN + local;
+      valid = local < kMxBN && row < g.N;
+      src = sb;
+      pitch = g.N;
     }
-    w[q] = v;
+    uint32_t w = 0;
+    if (valid) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int kb = 4 * ks + k;
+        if (kb < g.kblk) w |= static_cast<uint32_t>(__ldg(src + static_cast<int64_t>(kb) * pitch + row)) << (8 * k);
+      }
+    }
+    (is_a ? rec_a : rec_b)[rec * 128 + r * 4 + c] = w;
   }
 }
 
 __global__ void __launch_bounds__(kMxThreads, 1)
-    mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+    mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmRA, const __grid_constant__ CUtensorMap tmRB,
                       const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using L = MxLayout;
   constexpr int kBK = 128;
   constexpr int kKSteps = 4;
-  constexpr uint32_t kTx = L::kAStage + L::kBStage + L::kRawA + L::kRawB;
+  constexpr uint32_t kTxPair = 2 * (L::kAStage + L::kBStage + L::kSfA + L::kSfB);  // both CTAs' bytes
   constexpr uint32_t kTmemCols = 512;
   constexpr int kAccStride = 256;
+  constexpr uint16_t kBoth = 0x3;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -126,71 +178,81 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t sA = smem_addr(smem + L::kOffA);
   const uint32_t sB = smem_addr(smem + L::kOffB);
   const uint32_t sC = smem_addr(smem + L::kOffC);
-  const uint32_t sRawA = smem_addr(smem + L::kOffRawA);
-  const uint32_t sRawB = smem_addr(smem + L::kOffRawB);
   const uint32_t sSfA = smem_addr(smem + L::kOffSfA);
   const uint32_t sSfB = smem_addr(smem + L::kOffSfB);
   const uint32_t bar0 = smem_addr(smem + L::kOffBar);
   auto full_bar = [&](int s) { return bar0 + 8 * s; };
   auto empty_bar = [&](int s) { return bar0 + 8 * (kMxStages + s); };
-  auto sf_bar = [&](int s) { return bar0 + 8 * (2 * kMxStages + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8 * (3 * kMxStages + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8 * (3 * kMxStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8 * (3 * kMxStages + 4);
+  auto tfull_bar = [&](int a) { return bar0 + 8 * (2 * kMxStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8 * (2 * kMxStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8 * (2 * kMxStages + 4);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   uint32_t* last_par = misc + 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_cta_rank());
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
+  const int num_pair_tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
+  auto coord = [&](int tp) {
+    TileCoord c;
+    const int mp = tp / p.n_blocks;
+    c.nb = tp - mp * p.n_blocks;
+    c.mb = 2 * mp + rank;  // this CTA's 128-row block (past M: zero rows, clipped stores)
+    return c;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMxStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-      mbar_init(sf_bar(s), 1);
+      mbar_init(full_bar(s), 1);   // the even CTA's producer arms it for both CTAs' bytes
+      mbar_init(empty_bar(s), 1);  // one pair commit per round
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 32 * kMxEpiWarps);
+      mbar_init(tempty_bar(a), 2 * 32 * kMxEpiWarps);  // both CTAs' epilogue threads
     }
     mbar_init(drain_bar, 1);
     misc[1] = 0;
     fence_mbarrier_init();
   }
-  if (warp == 1) {
-    tmem_alloc(smem_addr(&misc[0]), kTmemCols);
-    tmem_relinquish();
+  if (warp == 1) {  // one warp in each CTA of the pair allocates together
+    tmem_alloc_pair(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
-      tma_prefetch_desc(&tmSA);
-      tma_prefetch_desc(&tmSB);
+      tma_prefetch_desc(&tmRA);
+      tma_prefetch_desc(&tmRB);
       int stage = 0, kstep = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(p, t);
+      for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
+        const TileCoord tc = coord(tp);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+          if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
             ok = false;
             break;
           }
           if (kstep != p.skip_kstep) {
-            const uint32_t fb = full_bar(stage);
-            mbar_arrive_expect_tx(fb, kTx);
-            tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
-            tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kMxBN, fb);
-            tma_load_2d(sRawA + stage * L::kRawA, &tmSA, tc.mb * kBM, kb * 4, fb);
-            tma_load_2d(sRawB + stage * L::kRawB, &tmSB, tc.nb * kMxBN, kb * 4, fb);
+            const uint32_t fb = map_to_cta(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
+            tma_load_2d_pair(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
+            tma_load_2d_pair(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kMxBN + rank * kMxBHalf, fb);
+            // records past the last M chunk read as zeros
+            tma_load_2d_pair(sSfA + stage * L::kSfA, &tmRA, 0, tc.mb * p.k_blocks + kb, fb);
+            tma_load_2d_pair(sSfB + stage * L::kSfB, &tmRB, 0, (tc.nb * p.k_blocks + kb) * 2, fb);
             issued |= 1u << stage;
             last_par[stage] = phase;
           }
@@ -201,117 +263,98 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
       }
       if (!ok) {
+        if (leader) {
+          for (int s = 0; s < kMxStages; ++s)
+            if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+        } else {
+          // this CTA's loads complete on the even CTA's barrier: give them time to land
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 2000000ull) {
+          }
+        }
+      } else {
+        // every pair commit to this CTA's empty barriers must land before exit
         for (int s = 0; s < kMxStages; ++s)
-          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+          if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
       }
     }
   } else if (warp == 1) {
-    // ---------------- scale-factor copies + MMA issuer ----------------
-    if (lane == 0) {
+    // ---------------- scale-factor copies + pair MMA issuer (even CTA) ----------------
+    if (lane == 0 && leader) {
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+      for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
-        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
+        if (!mbar_wait_cluster(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * kAccStride;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, wd, kWhereMmaFull) ||
-              !mbar_wait(sf_bar(stage), phase, wd, kWhereMmaSf)) {
+          if (!mbar_wait_cluster(full_bar(stage), phase, wd, kWhereMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t tsa = tmem_base + sf_col_a(stage);
           const uint32_t tsb = tmem_base + sf_col_b(stage);
-          tmem_cp_128x128b(tsa, sf_desc_a(sSfA + stage * L::kSfA));
-          tmem_cp_128x256b(tsb, sf_desc_b(sSfB + stage * L::kSfB));
+          tmem_cp_pair_32x128b_x4(tsa, rec_desc(sSfA + stage * L::kSfA));
+          tmem_cp_pair_32x128b_x4(tsb, rec_desc(sSfB + stage * L::kSfB));
+          tmem_cp_pair_32x128b_x4(tsb + 4, rec_desc(sSfB + stage * L::kSfB + kRec));
           const uint32_t a0 = sA + stage * L::kAStage;
           const uint32_t b0 = sB + stage * L::kBStage;
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k) {
-            mma_mxf8(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k),
-                     instr_desc_mx(kBM, kMxBN, k, k), tsa, tsb, (kb | k) != 0);
+            mma_mxf8_pair(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k),
+                          instr_desc_mx(2 * kBM, kMxBN, k, k), tsa, tsb, (kb | k) != 0);
           }
-          mma_commit(empty_bar(stage));
+          mma_commit_pair(empty_bar(stage), kBoth);
           if (++stage == kMxStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
+        mma_commit_pair(tfull_bar(acc), kBoth);
       }
-      if (!ok) {
-        mma_commit(drain_bar);
+      if (!ok) {  // let issued MMAs finish before TMEM is freed
+        mma_commit_pair(drain_bar, 0x1);
         mbar_wait_drain(drain_bar, 0, 200000000ull);
       }
     }
-  } else if (warp == 2) {
-    // ---------------- scale-factor regrouping ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      bool ok = true;
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        ok = mbar_wait(full_bar(stage), phase, wd, kWhereSfFull);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* rawA = smem + L::kOffRawA + stage * L::kRawA;
-        const uint8_t* rawB = smem + L::kOffRawB + stage * L::kRawB;
-        uint32_t wa[4], wb0[4], wb1[4];
-        sf_words(rawA, kBM, 0, kBM, lane, wa);
-        sf_words(rawB, kMxBN, 0, kMxBN, lane, wb0);
-        sf_words(rawB, kMxBN, 128, kMxBN, lane, wb1);
-        const uint32_t dA = sSfA + stage * L::kSfA;
-        const uint32_t dB = sSfB + stage * L::kSfB;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // the same words for lanes r + 32 q
-          const int l = 32 * q + lane;
-          st_shared_v4(dA + (l >> 3) * 128 + (l & 7) * 16, wa[0], wa[1], wa[2], wa[3]);
-          st_shared_v4(dB + (l >> 3) * 256 + (l & 7) * 16, wb0[0], wb0[1], wb0[2], wb0[3]);
-          st_shared_v4(dB + (l >> 3) * 256 + 128 + (l & 7) * 16, wb1[0], wb1[1], wb1[2], wb1[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sf_bar(stage));
-        if (++stage == kMxStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-      if (!ok) break;
-    }
   } else {
-    // ---------------- epilogue ----------------
-    const int ew = warp - 3;
-    const int quarter = warp & 3;
+    // ---------------- epilogue (both CTAs) ----------------
+    const int ew = warp - 2;                 // 0 .. 7
+    const int quarter = warp & 3;            // TMEM lanes this warp may access
+    const int col0 = ew < 4 ? 0 : 128;       // columns 0-127 or 128-223 of the tile
     const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
     int it = 0;
     uint32_t box = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-      const TileCoord tc = tile_coord(p, t);
+    for (int tp = pair; tp < num_pair_tiles; tp += npairs, ++it) {
+      const TileCoord tc = coord(tp);
       const int acc = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
       const int m_start = tc.mb * kBM + quarter * 32;
-      const int n_start = tc.nb * kMxBN;
-      const bool ok = mbar_wait(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
+      const int n_start = tc.nb * kMxBN + col0;
+      const bool ok = mbar_wait_cluster(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
-      epilogue_tile<kMxBN, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N, p.M,
-                                  lane, [&]() {
-                                    tc_fence_before();
-                                    mbar_arrive(tempty_bar(acc));
-                                  });
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride + col0;
+      const uint32_t release_bar = map_to_cta(tempty_bar(acc), 0);
+      auto release = [&]() {
+        tc_fence_before();
+        mbar_arrive_cluster(release_bar);
+      };
+      if (ew < 4)
+        epilogue_tile<128, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N, p.M, lane,
+                                  release);
+      else
+        epilogue_tile<kMxBN - 128, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N,
+                                          p.M, lane, release);
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -320,29 +363,60 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal it or use its TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
+}
+
+RecGeom rec_geom(int64_t M, int64_t N, int64_t K) {
+  RecGeom g;
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(N);
+  g.kblk = static_cast<int>(K / 32);
+  g.k_steps = static_cast<int>((K + 127) / 128);
+  g.m_chunks = static_cast<int>((M + kBM - 1) / kBM);
+  g.n_tiles = static_cast<int>((N + kMxBN - 1) / kMxBN);
+  return g;
 }
 
 }  // namespace
 
+size_t mxfp8_workspace_bytes(int64_t M_max, int64_t N, int64_t K) {
+  const RecGeom g = rec_geom(M_max, N, K);
+  return static_cast<size_t>(g.a_records() + g.b_records()) * kRec;
+}
+
 cudaError_t mxfp8_prepare() {
-  return cudaFuncSetAttribute(mxfp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(mxfp8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               MxLayout::kDynSmem);
 }
 
 sg_status_t mxfp8_launch(const LaunchArgs& a) {
-  CUtensorMap tmA, tmB, tmSA, tmSB, tmC;
-  const uint64_t kblk = static_cast<uint64_t>(a.K / 32);
+  const RecGeom g = rec_geom(a.M, a.N, a.K);
+  // B's records first: their count depends on N and K only, so A's (which grow
+  // with M) start at the same place for every M <= M_max.
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  uint32_t* rec_b = reinterpret_cast<uint32_t*>(ws);
+  uint32_t* rec_a = reinterpret_cast<uint32_t*>(ws + g.b_records() * kRec);
+  {
+    const int64_t words = (g.a_records() + g.b_records()) * 128;
+    const int64_t blocks = (words + 255) / 256;
+    const int grid = static_cast<int>(blocks < 4L * a.num_sms * 8 ? blocks : 4L * a.num_sms * 8);
+    mx_scale_records_kernel<<<grid, 256, 0, a.stream>>>(static_cast<const uint8_t*>(a.a_scale),
+                                                        static_cast<const uint8_t*>(a.b_scale), rec_a, rec_b, g);
+    const sg_status_t st = launch_status();
+    if (st != SG_OK) return st;
+  }
+  CUtensorMap tmA, tmB, tmRA, tmRB, tmC;
   if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, 128, kBM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kMxBN,
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kMxBHalf,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_scale, a.M, kblk, a.M, kBM, 4,
+      !encode_2d(&tmRA, CU_TENSOR_MAP_DATA_TYPE_UINT32, rec_a, kRec / 4, g.a_records(), kRec, kRec / 4, 1,
                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_2d(&tmSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_scale, a.N, kblk, a.N, kMxBN, 4,
+      !encode_2d(&tmRB, CU_TENSOR_MAP_DATA_TYPE_UINT32, rec_b, kRec / 4, g.b_records(), kRec, kRec / 4, 2,
                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols, kCBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_64B))
@@ -358,9 +432,28 @@ sg_status_t mxfp8_launch(const LaunchArgs& a) {
   p.skip_kstep = a.skip_kstep;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
-  mxfp8_gemm_kernel<<<grid, kMxThreads, MxLayout::kDynSmem, a.stream>>>(tmA, tmB, tmSA, tmSB, tmC, p);
-  return launch_status();
+  const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
+  const int max_pairs = a.num_sms / 2;
+  const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pairs * 2, 1, 1);
+  cfg.blockDim = dim3(kMxThreads, 1, 1);
+  cfg.dynamicSmemBytes = MxLayout::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mxfp8_pair_kernel, tmA, tmB, tmRA, tmRB, tmC, p);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    cudaGetLastError();  // clear the non-sticky launch error
+    return SG_ERR_CUDA;
+  }
+  return SG_OK;
 }
 
 void mxfp8_config(TileConfig* c) {
@@ -368,6 +461,8 @@ void mxfp8_config(TileConfig* c) {
   c->bn = kMxBN;
   c->bk = 128;
   c->stages = kMxStages;
+  c->cluster = 2;
+  c->rows_per_group = 2 * kBM;
 }
 
 }  // namespace sg

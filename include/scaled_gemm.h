@@ -39,17 +39,19 @@
  * Shape rules (checked on the host before anything is launched):
  *   0 <= M <= M_max (M == 0 or N == 0 launches nothing), N % 16 == 0,
  *   K % 16 == 0 (ptpc), K % 8 == 0 (bf16), K % 128 == 0 (blockscale),
- *   K % 32 == 0 and M % 16 == 0 (mxfp8: the K-block-major scale rows are
- *   fetched by TMA, whose row pitch must be a multiple of 16 bytes),
- *   M, N, K < 2^31.  K == 0 writes C = 0.
+ *   K % 32 == 0 (mxfp8), M, N, K < 2^31.  K == 0 writes C = 0.
  *
  * Errors: every call returns an sg_status_t and never aborts or prints (set the
  * environment variable SG_DEBUG=1 to log rejected calls to stderr).  Kernel faults,
  * like any CUDA asynchronous error, surface at the caller's next synchronisation.
  *
  * Streams: scaled_gemm_launch is asynchronous on `stream` and never synchronises.
- * A handle is immutable after creation, so launches on one handle from several host
- * threads or streams are safe; destroying a handle must not race a launch on it.
+ * A ptpc, blockscale or bf16 handle is immutable after creation, so launches on one
+ * such handle from several host threads or streams are safe.  An mxfp8 handle owns
+ * a device workspace (its launch first rearranges the scales there for the tensor
+ * core), so launches on one mxfp8 handle must be ordered: issue them on one stream,
+ * or order their streams, or use one handle per stream.  Destroying a handle must
+ * not race a launch on it.
  */
 #ifndef SCALED_GEMM_H
 #define SCALED_GEMM_H
@@ -85,7 +87,9 @@ typedef enum {
 
 /* Create a plan for one (mode, N, K) that serves any M <= M_max on `device`
  * (-1 = the current device).  The plan holds a 16-byte device status word, set
- * up here, that kernels write only when a wait times out.
+ * up here, that kernels write only when a wait times out; an mxfp8 plan also
+ * allocates here its scale workspace, (ceil(M_max/128) + 2 ceil(N/224)) *
+ * ceil(K/128) * 512 bytes of device memory.
  * On success *out receives the handle; on failure *out is set to NULL.
  * Cited: ROCm/mori PR 809, "Using it" (one instance serves one (n, k) and any M
  * up to m_max; bad configuration is refused at construction).                   */
@@ -106,9 +110,10 @@ sg_status_t scaled_gemm_destroy(sg_handle_t h);
 /* A static English description of a status code. */
 const char* scaled_gemm_status_string(sg_status_t s);
 
-/* Tile geometry the plan launches with: BM x BN output tiles, BK elements of K per
- * pipeline stage, `stages` shared-memory stages, `grid` persistent CTAs for M = M_max.
- * Any output pointer may be NULL.                                                */
+/* Tile geometry the plan launches with: BM x BN output tiles per CTA, BK elements
+ * of K per pipeline stage, `stages` shared-memory stages, `grid` persistent CTAs for
+ * M = M_max (whole clusters, where the kernel runs CTAs in pairs).  Any output
+ * pointer may be NULL.                                                           */
 sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int* stages, int* grid);
 
 /* Read and clear the plan's device status word: synchronises `stream`, then stores

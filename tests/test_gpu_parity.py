@@ -119,10 +119,13 @@ def test_m_zero_is_a_no_op(gpu):
     "M,N,K",
     [
         (16, 16, 32),       # one partial K block (1 of 4 scale blocks)
+        (1, 16, 64),        # one row: the pair's second CTA reads only zero-filled rows
         (128, 224, 128),    # one tile
         (144, 240, 416),    # ragged M, N and K (K = 3.25 stages)
         (256, 512, 1792),
         (384, 7168, 256),   # the full weight width, two K blocks
+        (200, 448, 1024),   # M not a multiple of 16
+        (383, 672, 2080),   # odd number of 128-row chunks, ragged last K step (65 scale blocks)
     ],
 )
 def test_mxfp8_shapes(gpu, M, N, K):
