@@ -7,22 +7,28 @@
 // "Not done yet") and per 128 x 128 block of B (ROCm/mori PR 785, cost table:
 // the "blockscale" mode).  The tensor core's block-scaled MMA accepts only
 // power-of-two (e8m0) or e4m3 scale factors, so arbitrary fp32 scales cannot be
-// fed to it.  Instead every K block's product P_j goes into its own TMEM
-// buffer, and "promotion" warps read it with tcgen05.ld, multiply by the two
-// scales and add it to an fp32 accumulator held in registers.
+// fed to it.  Instead every K block's product P_j goes into a TMEM buffer, and
+// "promotion" warps read it with tcgen05.ld, multiply by the two scales and add
+// it to an fp32 accumulator held in registers.
 //
-// Per CTA (one per SM, persistent over 128 x 128 output tiles, so one B scale
-// block per tile):
-//   warp 0      TMA producer (A, B tiles into a 5-stage ring).
-//   warp 1      TMEM owner and MMA issuer: for K block j, wait full[s] and
-//               part_empty[p], 4 MMAs into partial buffer p (128 columns, 4
+// Per CTA (one per SM, persistent over 128 x 256 output tiles: one N = 256 MMA
+// per K step, where 128-wide tiles ran 1.56x slower per FLOP; the tile covers
+// two B scale blocks, one per half):
+//   warpgroup 0 (120 registers a thread after setmaxnreg.dec):
+//     warp 0    TMA producer (A, B tiles into a 4-stage ring).
+//     warp 1    TMEM owner and MMA issuer: for K block j, wait full[s] and
+//               part_empty[p], 4 MMAs into partial buffer p (256 columns, 2
 //               buffers cycling across K blocks and tiles), commit empty[s] and
 //               part_full[p].
-//   warps 2-9   promotion + epilogue: 2 warps per TMEM lane quarter, 64 columns
-//               each; per K block wait part_full[p], tcgen05.ld, release the
-//               buffer (tcgen05.fence::before_thread_sync + arrive part_empty[p]),
-//               acc += P * (sa * sb); after the last block round to bf16 and
-//               store through shared memory and TMA.
+//   warpgroups 1-2 (192 registers a thread after setmaxnreg.inc): promotion +
+//     epilogue, 2 warps per TMEM lane quarter, 128 columns (one B scale block)
+//     each; per K block wait part_full[p], read the buffer in two 64-column
+//     halves, release it after the second (tcgen05.fence::before_thread_sync +
+//     arrive part_empty[p]), acc += P * (sa * sb) with packed f32x2 FMAs; after
+//     the last block round to bf16 and store through shared memory and TMA.
+//     The 128 accumulators of a thread are why the register split exists.
+// The register split adds up to the launch allocation exactly (384 threads x 168
+// registers), so setmaxnreg.inc never waits for registers that cannot come.
 // The scales are loaded from global memory four K blocks ahead of their use.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -34,12 +40,18 @@ namespace sg {
 
 namespace {
 
-constexpr int kBsBN = 128;
-constexpr int kBsStages = 5;
-constexpr int kBsParts = 4;
-constexpr int kBsWarps = 8;  // promotion warps
-constexpr int kBsThreads = 64 + 32 * kBsWarps;
-constexpr int kBsCols = 64;  // columns per promotion warp
+constexpr int kBsBN = 256;
+constexpr int kBsStages = 4;
+constexpr int kBsParts = 2;
+constexpr int kBsWarps = 8;                          // promotion warps
+constexpr int kBsThreads = 128 + 32 * kBsWarps;      // warpgroup 0 + two promotion warpgroups
+constexpr int kBsCols = 128;                         // columns per promotion warp
+constexpr int kBsLaunchRegs = 168;                   // 65536 / 384, rounded down to 8
+constexpr int kBsRegsCtl = 120;
+constexpr int kBsRegsPromo = 192;
+static_assert(4 * kBsRegsCtl + 8 * kBsRegsPromo == 12 * kBsLaunchRegs,
+              "the register split must equal the launch allocation");
+static_assert(kBsThreads * kBsLaunchRegs <= 65536, "launch allocation");
 
 struct BsLayout {
   static constexpr int kAStage = kBM * kRowBytes;
@@ -52,8 +64,16 @@ struct BsLayout {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 4 * kBsStages;
   static constexpr int kDynSmem = kBytes + 1024;
-  static_assert(kOffC % 1024 == 0, "alignment");
+  static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "alignment");
+  static_assert(kDynSmem <= 232448, "shared memory");
 };
+
+__device__ __forceinline__ void regs_dec_ctl() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBsRegsCtl));
+}
+__device__ __forceinline__ void regs_inc_promo() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBsRegsPromo));
+}
 
 __global__ void __launch_bounds__(kBsThreads, 1)
     blockscale_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -107,9 +127,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
+  if (warp < 4) {
+    regs_dec_ctl();
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer ----------------
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       int stage = 0, kstep = 0;
@@ -139,10 +160,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         for (int s = 0; s < kBsStages; ++s)
           if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
       }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: one TMEM partial per K block ----------------
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- MMA issuer: one TMEM partial per K block ----------------
       int stage = 0, part = 0;
       uint32_t phase = 0, ppar = 0;
       bool ok = true;
@@ -178,40 +197,45 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       }
     }
   } else {
+    regs_inc_promo();
     // ---------------- promotion + epilogue ----------------
-    const int ew = warp - 2;           // 0..7
+    const int ew = warp - 4;           // 0..7
     const int quarter = warp & 3;
-    const int col0 = (ew >> 2) * kBsCols;
+    const int half = ew >> 2;          // which 128-column half of the tile (= B scale block)
+    const int col0 = half * kBsCols;
     const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
     const int kblocks = p.k_blocks;
+    const int nsb = (p.N + 127) / 128;  // B scale blocks along N
     int part = 0;
     uint32_t ppar = 0, box = 0;
     bool ok = true;
-    // Scale products s = sa[j][row] * sb[nb][j] are loaded kScaleAhead K blocks
+    // Scale products s = sa[j][row] * sb[n/128][j] are loaded kScaleAhead K blocks
     // before they are needed (a ring of registers), and the first ones of the next
     // tile are loaded before this tile's epilogue, so no promotion step waits on
-    // a global load.  The accumulator is 32 packed fp32 pairs, updated with one
+    // a global load.  The accumulator is 64 packed fp32 pairs, updated with one
     // f32x2 FMA per pair.
     constexpr int kScaleAhead = 4;
     float ring_a[kScaleAhead], ring_b[kScaleAhead];
     const float* sa_base = p.a_scale;
     const float* sb_base = p.b_scale;
-    bool row_ok = false;
-    auto tile_scale_ptrs = [&](int t, const float*& sa_ptr, const float*& sb_ptr) {
-      const TileCoord c = tile_coord(p, t);
-      const int row = c.mb * kBM + quarter * 32 + lane;
-      row_ok = row < p.M;
-      sa_ptr = sa_base + (row_ok ? row : 0);
-      sb_ptr = sb_base + static_cast<int64_t>(c.nb) * kblocks;
-    };
+    bool row_ok = false, col_ok = false;
     const float* sa_ptr = sa_base;
     const float* sb_ptr = sb_base;
+    auto tile_scale_ptrs = [&](int t) {
+      const TileCoord c = tile_coord(p, t);
+      const int row = c.mb * kBM + quarter * 32 + lane;
+      const int sbr = 2 * c.nb + half;  // this warp's B scale block
+      row_ok = row < p.M;
+      col_ok = sbr < nsb;               // past N: the columns are clipped at the store
+      sa_ptr = sa_base + (row_ok ? row : 0);
+      sb_ptr = sb_base + static_cast<int64_t>(col_ok ? sbr : 0) * kblocks;
+    };
     auto load_scales = [&](int kb, float& a_out, float& b_out) {
       a_out = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.M) : 0.f;
-      b_out = __ldg(sb_ptr + kb);
+      b_out = col_ok ? __ldg(sb_ptr + kb) : 0.f;
     };
     if (static_cast<int>(blockIdx.x) < p.num_tiles) {
-      tile_scale_ptrs(blockIdx.x, sa_ptr, sb_ptr);
+      tile_scale_ptrs(blockIdx.x);
 #pragma unroll
       for (int d = 0; d < kScaleAhead; ++d)
         if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
@@ -238,16 +262,21 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             tc_fence_after();
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + part * kBsBN + col0;
-            uint32_t v0[32], v1[32];
-            tmem_ld_32x32b_x32(taddr, v0);
-            tmem_ld_32x32b_x32(taddr + 32, v1);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(pempty_bar(part));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              acc[j] = fma_f32x2(pack_f32x2(v0[2 * j], v0[2 * j + 1]), s2, acc[j]);
-              acc[16 + j] = fma_f32x2(pack_f32x2(v1[2 * j], v1[2 * j + 1]), s2, acc[16 + j]);
+            for (int h = 0; h < 2; ++h) {  // two 64-column halves; release after the second
+              uint32_t v0[32], v1[32];
+              tmem_ld_32x32b_x32(taddr + 64 * h, v0);
+              tmem_ld_32x32b_x32(taddr + 64 * h + 32, v1);
+              tmem_wait_ld();
+              if (h == 1) {
+                tc_fence_before();
+                mbar_arrive(pempty_bar(part));
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                acc[32 * h + j] = fma_f32x2(pack_f32x2(v0[2 * j], v0[2 * j + 1]), s2, acc[32 * h + j]);
+                acc[32 * h + 16 + j] = fma_f32x2(pack_f32x2(v1[2 * j], v1[2 * j + 1]), s2, acc[32 * h + 16 + j]);
+              }
             }
             if (++part == kBsParts) {
               part = 0;
@@ -260,14 +289,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       // the next tile's first scales load while this tile is stored
       const int tn = t + static_cast<int>(gridDim.x);
       if (tn < p.num_tiles) {
-        tile_scale_ptrs(tn, sa_ptr, sb_ptr);
+        tile_scale_ptrs(tn);
 #pragma unroll
         for (int d = 0; d < kScaleAhead; ++d)
           if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
       }
       const int n_start = tc.nb * kBsBN + col0;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kBsCols / 32; ++h) {
         uint32_t packed[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {

@@ -537,7 +537,6 @@ struct DenseKernel {
   static constexpr bool kPair = false;
   static constexpr int kThreads = 64 + 32 * EPI_WARPS;
   static constexpr int kCluster = CLUSTER;
-  static constexpr int kStages = STAGES;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
   }
@@ -549,7 +548,6 @@ struct PairKernel {
   static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX>;
   static constexpr int kThreads = 64 + 32 * EPI_WARPS;
   static constexpr int kCluster = 2;
-  static constexpr int kStages = STAGES;
   static constexpr int kBoxW = 32;
   static constexpr bool kPair = true;
   static cudaError_t prepare() {
@@ -559,10 +557,12 @@ struct PairKernel {
 
 // Long K: pair MMA (cta_group::2) on 256 x 256 tiles.  Short K: pairs of CTAs on
 // vertically adjacent 128 x 256 tiles that share (multicast) each B tile.
+constexpr int kLongKStages = 5;
+constexpr int kShortKStages = 3;
 template <int MODE>
-using LongK = PairKernel<MODE, 5, 8, 2>;
+using LongK = PairKernel<MODE, kLongKStages, 8, 2>;
 template <int MODE>
-using ShortK = DenseKernel<MODE, 3, 8, 2, 2, 32>;
+using ShortK = DenseKernel<MODE, kShortKStages, 8, 2, 2, 32>;
 
 int dense_bk(int mode) { return mode == kModeBf16 ? 64 : 128; }
 
@@ -651,7 +651,7 @@ void dense_config(int mode, int64_t K, TileConfig* c) {
   c->bm = kBM;
   c->bn = kDenseBN;
   c->bk = dense_bk(mode);
-  c->stages = short_k(mode, K) ? ShortK<kModePtpc>::kStages : LongK<kModePtpc>::kStages;
+  c->stages = short_k(mode, K) ? kShortKStages : kLongKStages;
   c->cluster = 2;  // both paths: pairs (pair MMA for long K, shared B for short K)
   c->rows_per_group = 2 * kBM;
 }
