@@ -305,7 +305,7 @@ def run_gpu(args, control, rank, local):
     roofline = {
         "bound": "tensor", "achieved": round(achieved, 1), "peak": round(dom_peak, 1), "unit": "TFLOP/s",
         "frac": round(achieved / dom_peak, 3), "traffic": traffic,
-        "kernel": ("dense_gemm_kernel<ptpc>" if pc["mode"] == "ptpc" else pc["mode"] + "_gemm_kernel"),
+        "kernel": kernel_name(pc["mode"], pc["K"]),
         "workload": dom,
         "peak_source": "%s: 2 x bf16_tflops_sustained (fp8 = 2 x bf16 nominal ratio)" % peak_kind,
     }
@@ -335,6 +335,7 @@ def run_gpu(args, control, rank, local):
         status_bad += code != 0
 
     quant = None if args.no_quant else run_quantize(binding, dev, stream, hbm)
+    extra = None if (args.no_quant or args.only) else run_extra(binding, dev, stream, local, fp8_peak)
 
     # end to end through the C ABI with host buffers: H2D inputs, GEMM, D2H C
     e2e = None if args.no_e2e else run_e2e(work, launch, stream, args, control, dev)
@@ -364,10 +365,11 @@ def run_gpu(args, control, rank, local):
         },
         "roofline": roofline,
         "quantize": quant,
+        "extra": extra,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clk,
-        "gpu_launches": args.steps * n,
+        "gpu_launches": args.steps * sum(KERNELS_PER_LAUNCH.get(d["case"].mode, 1) for d in work),
         "bad_launches": {"per_workload": 0 if args.no_bad_check else 20, "workloads": n, "bad": bad,
                          "watchdog_timeouts": status_bad},
         "per_config": per,
@@ -376,6 +378,53 @@ def run_gpu(args, control, rank, local):
                   "bf16_tflops_sustained": bf16_peak, "hbm_gbs": hbm},
     }
     return line
+
+
+# Kernels one scaled_gemm_launch enqueues: mxfp8 rearranges its scales first.
+KERNELS_PER_LAUNCH = {"mxfp8": 2}
+
+
+def kernel_name(mode, K):
+    """The kernel that runs a (mode, K) launch."""
+    if mode == "mxfp8":
+        return "mxfp8_pair_kernel"
+    if mode == "blockscale":
+        return "blockscale_gemm_kernel"
+    short = (K + (63 if mode == "bf16" else 127)) // (64 if mode == "bf16" else 128) <= 4
+    return ("dense_gemm_kernel<%s, short K>" if short else "dense_pair_kernel<%s>") % mode
+
+
+def run_extra(binding, dev, stream, local, fp8_peak, iters=20):
+    """Shapes outside the suite (not part of `value`), each timed on its own:
+    3 warm-up launches, then `iters` launches between CUDA events; inputs plus
+    output are larger than L2."""
+    out = {}
+    sraw = stream.cuda_stream
+    for name in synth.EXTRA:
+        mode, M, N, K, seed, a_std, b_std = synth.CONFIGS[name]
+        c = synth.make_case(mode, M, N, K, seed=seed, a_std=a_std, b_std=b_std)
+        A, B = c.A.to(dev), c.B.to(dev)
+        sa, sb = c.sa.to(dev), c.sb.to(dev)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        h = binding.scaled_gemm_create(mode, N, K, M, local)
+        f = lambda: binding.scaled_gemm_launch(h, A.data_ptr(), B.data_ptr(), sa.data_ptr(), sb.data_ptr(),  # noqa: E731
+                                               C.data_ptr(), M, sraw)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                f()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(iters):
+                f()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / iters
+        tf = c.flops / (us * 1e-6) / 1e12
+        out[name] = {"mode": mode, "M": M, "N": N, "K": K, "us": round(us, 2), "tflops": round(tf, 1),
+                     "frac_peak": round(tf / fp8_peak, 3), "kernel": kernel_name(mode, K)}
+        binding.scaled_gemm_destroy(h)
+        del A, B, sa, sb, C
+    return out
 
 
 def run_quantize(binding, dev, stream, hbm, R=32768, C=7168, iters=20):
@@ -586,7 +635,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--no-quant", action="store_true", help="skip the quantisation measurement (profiling runs)")
     ap.add_argument("--no-bad-check", action="store_true", help="skip the 20-launch check (profiling runs)")
-    ap.add_argument("--only", default=None, choices=synth.SUITE, help="one workload (profiling runs)")
+    ap.add_argument("--only", default=None, choices=synth.SUITE + synth.EXTRA, help="one workload (profiling runs)")
     ap.add_argument("--rows", type=int, default=None, help="override M of the workload(s) (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       // ---------------- TMA producer ----------------
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      const uint64_t keep_b = l2_policy_evict_last();
       int stage = 0, kstep = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           if (kstep != p.skip_kstep) {
             mbar_arrive_expect_tx(full_bar(stage), kTx);
             tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
-            tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kBsBN, full_bar(stage));
+            tma_load_2d_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kBsBN, full_bar(stage), keep_b);
             issued |= 1u << stage;
             last_par[stage] = phase;
           }

@@ -68,6 +68,7 @@ __device__ __forceinline__ uint32_t cbox_chunk_addr(uint32_t box, int row, int c
 // still be reading shared memory.  Every writer fences its generic stores into
 // the async proxy before lane 0 issues the TMA store (deepseek-ai/DeepGEMM
 // PR 453, Fix: the fence is executed by all threads, not only the issuing one).
+// The output is stored with the evict-first L2 policy: it is not read again.
 template <int NBOX = 2, int W = 32>
 __device__ __forceinline__ void store_box(uint32_t bufs, uint32_t& box, const uint32_t (&packed)[W / 2],
                                           const CUtensorMap* tmC, int x, int y, int N, int M, int lane) {
@@ -84,7 +85,7 @@ __device__ __forceinline__ void store_box(uint32_t bufs, uint32_t& box, const ui
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (x < N && y < M) tma_store_2d(tmC, buf, x, y);
+    if (x < N && y < M) tma_store_2d_hint(tmC, buf, x, y, l2_policy_evict_first());
     bulk_commit_group();
   }
 }

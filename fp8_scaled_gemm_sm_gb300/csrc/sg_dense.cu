@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      const uint64_t keep_b = l2_policy_evict_last();
       int stage = 0, kstep = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
@@ -393,7 +394,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             const uint32_t fb = map_to_cta(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
             tma_load_2d_pair(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
-            tma_load_2d_pair(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN + rank * (BN / 2), fb);
+            tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN + rank * (BN / 2), fb,
+                                  keep_b);
             issued |= 1u << stage;
             last_par[stage] = phase;
           }

@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      const uint64_t keep_b = l2_policy_evict_last();
       tma_prefetch_desc(&tmRA);
       tma_prefetch_desc(&tmRB);
       int stage = 0, kstep = 0;
@@ -249,7 +250,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const uint32_t fb = map_to_cta(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
             tma_load_2d_pair(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
-            tma_load_2d_pair(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kMxBN + rank * kMxBHalf, fb);
+            tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kMxBN + rank * kMxBHalf, fb,
+                                  keep_b);
             // records past the last M chunk read as zeros
             tma_load_2d_pair(sSfA + stage * L::kSfA, &tmRA, 0, tc.mb * p.k_blocks + kb, fb);
             tma_load_2d_pair(sSfB + stage * L::kSfB, &tmRB, 0, (tc.nb * p.k_blocks + kb) * 2, fb);

@@ -9,6 +9,7 @@ it produces.
 from .gen import (  # noqa: F401
     Case,
     SUITE,
+    EXTRA,
     CONFIGS,
     make_case,
     make_int_case,

@@ -103,6 +103,11 @@ def test_fullsize_workload(gpu, name):
     _run(gpu, name)
 
 
+@pytest.mark.parametrize("name", synth.EXTRA)
+def test_fullsize_extra_shape(gpu, name):
+    _run(gpu, name)
+
+
 def test_fullsize_bf16_1000_launches_bit_identical(gpu):
     _run(gpu, "c4_bf16_4096x896x1024", launches=1000)
 
