@@ -139,6 +139,42 @@ def gemm_points(mode, A, B, sa, sb, ms, ns):
     return R, ref
 
 
+def gather_source(idx, rows_src):
+    """For each output row of a gather-GEMM, the source row it reads and whether
+    that row exists.  An index outside [0, rows_src) names no row: the output row
+    reads row 0 with scale 0, so it is zero (this project's reading; ROCm/aiter
+    PR 6539, Technical Details, names the gather_kv_b_proj kernel without fixing
+    what a bad index does)."""
+    idx = np.asarray(idx, dtype=np.int64)
+    valid = (idx >= 0) & (idx < rows_src)
+    return np.where(valid, idx, 0), valid
+
+
+def gemm_gather(A_src, idx, B, sa_src, sb, rows=None, want_r=True):
+    """Gather-GEMM in ptpc mode: output row i is the ptpc GEMM row of source row
+    idx[i] of A_src [R, K] (e4m3) with its per-row scale sa_src[idx[i]], against B
+    [N, K] with per-channel scales sb -- the gather of rows by index that
+    gather_kv_b_proj fuses in front of the projection GEMM (ROCm/aiter PR 6539,
+    Motivation and Technical Details).  The gather is numpy indexing; the GEMM is
+    ``gemm("ptpc", ...)`` on the gathered rows.  Returns ``(R, ref)`` as gemm."""
+    A_src = np.ascontiguousarray(A_src, dtype=np.uint8)
+    sa_src = np.ascontiguousarray(sa_src, dtype=np.float32)
+    src, valid = gather_source(idx, A_src.shape[0])
+    A = A_src[src]
+    sa = np.where(valid, sa_src[src], np.float32(0)).astype(np.float32)
+    return gemm("ptpc", A, B, sa, sb, rows=rows, want_r=want_r)
+
+
+def gemm_gather_points(A_src, idx, B, sa_src, sb, ms, ns):
+    """Elements (ms[j], ns[j]) of the gather-GEMM, computed one by one."""
+    A_src = np.ascontiguousarray(A_src, dtype=np.uint8)
+    sa_src = np.ascontiguousarray(sa_src, dtype=np.float32)
+    src, valid = gather_source(idx, A_src.shape[0])
+    A = A_src[src]
+    sa = np.where(valid, sa_src[src], np.float32(0)).astype(np.float32)
+    return gemm_points("ptpc", A, B, sa, sb, ms, ns)
+
+
 def bits_to_f64(bits) -> np.ndarray:
     """bf16 bit patterns (uint16) -> float64 values, via the oracle's own decoder rule."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16

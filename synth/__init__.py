@@ -12,6 +12,10 @@ from .gen import (  # noqa: F401
     EXTRA,
     CONFIGS,
     make_case,
+    GatherCase,
+    make_gather_case,
+    paged_indices,
+    GATHER_CONFIGS,
     make_int_case,
     quantize_e4m3_rows,
     quantize_e4m3_blocks_1x128,

@@ -171,6 +171,72 @@ def make_int_case(M: int, N: int, K: int, lo: int = -16, hi: int = 16, seed: int
     )
 
 
+@dataclasses.dataclass
+class GatherCase:
+    """One gather-GEMM problem (ptpc): output row i reads row idx[i] of A_src.
+
+    A_src uint8 e4m3 [R, K] with per-row scales sa_src fp32 [R]; idx int32 [M];
+    B uint8 e4m3 [N, K] with per-channel scales sb fp32 [N]."""
+
+    M: int
+    N: int
+    K: int
+    R: int
+    A_src: torch.Tensor
+    sa_src: torch.Tensor
+    idx: torch.Tensor
+    B: torch.Tensor
+    sb: torch.Tensor
+    seed: int = 0
+    mode: str = "ptpc"
+
+    def numpy(self):
+        """(A_src, idx, B, sa_src, sb) as numpy arrays."""
+        return self.A_src.numpy(), self.idx.numpy(), self.B.numpy(), self.sa_src.numpy(), self.sb.numpy()
+
+    @property
+    def flops(self) -> float:
+        return gemm_flops(self.M, self.N, self.K)
+
+
+def paged_indices(M: int, R: int, page: int, g: torch.Generator, min_len: int = 64, max_len: int = 2048) -> torch.Tensor:
+    """Row indices of M tokens read from a paged cache of R rows: sequences of
+    lengths drawn uniformly from [min_len, max_len] (the last one cut to fit),
+    each stored in pages of `page` rows taken from a shuffled free list, read in
+    order.  int32 [M]."""
+    free = torch.randperm(R // page, generator=g)
+    out, used, left = [], 0, M
+    while left > 0:
+        n = min(left, int(torch.randint(min_len, max_len + 1, (1,), generator=g)))
+        npages = (n + page - 1) // page
+        if used + npages > free.numel():
+            raise ValueError("cache of %d rows too small for %d gathered rows" % (R, M))
+        pages = free[used:used + npages]
+        used += npages
+        out.append((pages[:, None] * page + torch.arange(page)[None, :]).reshape(-1)[:n])
+        left -= n
+    return torch.cat(out).to(torch.int32).contiguous()
+
+
+def make_gather_case(M: int, R: int, N: int, K: int, seed: int = 0, b_std: float = 0.02,
+                     page: int = 64) -> GatherCase:
+    """Seeded gather-GEMM case: A_src ~ N(0,1) [R, K] quantised per row, B ~ N(0, b_std)
+    [N, K] quantised per output channel (drawn in that order), then paged indices."""
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    qa, sa = quantize_e4m3_rows(_draw(g, R, K, 1.0))
+    qb, sb = quantize_e4m3_rows(_draw(g, N, K, b_std))
+    idx = paged_indices(M, R, page, g)
+    return GatherCase(M, N, K, R, qa.contiguous(), sa, idx, qb.contiguous(), sb, seed)
+
+
+# The gather-GEMM workload: a KV projection of 32 heads x (128 + 128) columns over
+# a 512-wide latent, for 16384 tokens gathered from a 65536-row paged cache.
+GATHER_CONFIGS = {
+    "g_ptpc_gather_16384x8192x512": (16384, 65536, 8192, 512, 0),
+}
+
+
 def gemm_flops(M, N, K) -> float:
     return 2.0 * M * N * K
 
