@@ -397,7 +397,9 @@ def kernel_name(mode, K):
 def run_extra(binding, dev, stream, local, fp8_peak, iters=20):
     """Shapes outside the suite (not part of `value`), each timed on its own:
     3 warm-up launches, then `iters` launches between CUDA events; inputs plus
-    output are larger than L2."""
+    output are larger than L2.  Includes the gather-GEMM workload (16384 rows
+    gathered from a 65536-row paged cache, N = 8192, K = 512) through
+    scaled_gemm_launch_gather."""
     out = {}
     sraw = stream.cuda_stream
     for name in synth.EXTRA:
@@ -424,6 +426,31 @@ def run_extra(binding, dev, stream, local, fp8_peak, iters=20):
                      "frac_peak": round(tf / fp8_peak, 3), "kernel": kernel_name(mode, K)}
         binding.scaled_gemm_destroy(h)
         del A, B, sa, sb, C
+    for name, (M, R, N, K, seed) in synth.GATHER_CONFIGS.items():
+        c = synth.make_gather_case(M, R, N, K, seed=seed)
+        A, sa, idx = c.A_src.to(dev), c.sa_src.to(dev), c.idx.to(dev)
+        B, sb = c.B.to(dev), c.sb.to(dev)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        h = binding.scaled_gemm_create("ptpc", N, K, M, local)
+        f = lambda: binding.scaled_gemm_launch_gather(h, A.data_ptr(), R, idx.data_ptr(), B.data_ptr(),  # noqa: E731
+                                                      sa.data_ptr(), sb.data_ptr(), C.data_ptr(), M, sraw)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                f()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(iters):
+                f()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / iters
+        tf = c.flops / (us * 1e-6) / 1e12
+        byts = M * K + N * K + 2.0 * M * N + 4.0 * (2 * M + N)  # gathered A, B, C, a/b scales, idx
+        out[name] = {"mode": "ptpc gather", "M": M, "N": N, "K": K, "R": R, "us": round(us, 2),
+                     "tflops": round(tf, 1), "frac_peak": round(tf / fp8_peak, 3),
+                     "gbs": round(byts / (us * 1e-6) / 1e9, 1), "kernel": "dense_gemm_kernel<ptpc, gather>"}
+        binding.scaled_gemm_destroy(h)
+        del A, sa, idx, B, sb, C
     return out
 
 

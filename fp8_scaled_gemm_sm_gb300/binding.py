@@ -29,6 +29,7 @@ _int = ctypes.c_int
 SIGNATURES = {
     "scaled_gemm_create": (_int, [ctypes.POINTER(_vp), _int, _i64, _i64, _i64, _int]),
     "scaled_gemm_launch": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "scaled_gemm_launch_gather": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "scaled_gemm_destroy": (_int, [_vp]),
     "scaled_gemm_status_string": (ctypes.c_char_p, [_int]),
     "scaled_gemm_get_config": (_int, [_vp] + [ctypes.POINTER(_int)] * 5),
@@ -87,6 +88,15 @@ def scaled_gemm_launch(h, A, B, a_scale, b_scale, C, M, stream=0):
     _check(
         lib().scaled_gemm_launch(h, A, B, a_scale or None, b_scale or None, C, int(M), stream or None),
         "scaled_gemm_launch",
+    )
+
+
+def scaled_gemm_launch_gather(h, A_src, R, idx, B, a_scale_src, b_scale, C, M, stream=0):
+    """Gather-GEMM on a ptpc plan: row i of C from source row idx[i] of A_src (see the C header)."""
+    _check(
+        lib().scaled_gemm_launch_gather(h, A_src or None, int(R), idx or None, B or None, a_scale_src or None,
+                                        b_scale or None, C or None, int(M), stream or None),
+        "scaled_gemm_launch_gather",
     )
 
 

@@ -302,6 +302,59 @@ sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, cons
   return r == SG_OK ? SG_OK : fail(r, "launch: kernel launch");
 }
 
+sg_status_t scaled_gemm_launch_gather(sg_handle_t h, const void* A_src, int64_t R, const int32_t* idx,
+                                      const void* B, const void* a_scale_src, const void* b_scale,
+                                      void* C, int64_t M, sg_stream_t stream) {
+  if (!h) return fail(SG_ERR_INVALID_ARG, "launch_gather: NULL handle");
+  if (h->mode != SG_MODE_PTPC) return fail(SG_ERR_INVALID_ARG, "launch_gather: the plan is not ptpc");
+  if (M < 0 || M > h->M_max) return fail(SG_ERR_INVALID_ARG, "launch_gather: M outside [0, M_max]");
+  if (R < 0) return fail(SG_ERR_INVALID_ARG, "launch_gather: negative R");
+  if (R > kMaxDim) return fail(SG_ERR_UNSUPPORTED_SHAPE, "launch_gather: R >= 2^31");
+  if (M == 0 || h->N == 0) return SG_OK;
+  if (!C) return fail(SG_ERR_INVALID_ARG, "launch_gather: C is NULL");
+  if (!aligned16(C)) return fail(SG_ERR_MISALIGNED, "launch_gather: C");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (h->K == 0 || R == 0) {  // empty contraction, or no source row: C = 0
+    return cudaMemsetAsync(C, 0, static_cast<size_t>(M) * h->N * 2, s) == cudaSuccess
+               ? SG_OK
+               : fail(SG_ERR_CUDA, "launch_gather: memset");
+  }
+  if (!A_src || !idx || !B || !a_scale_src || !b_scale)
+    return fail(SG_ERR_INVALID_ARG, "launch_gather: NULL operand");
+  if (!aligned16(A_src) || !aligned16(idx) || !aligned16(B) || !aligned16(a_scale_src) || !aligned16(b_scale))
+    return fail(SG_ERR_MISALIGNED, "launch_gather: operand");
+  auto overlap = [](const void* p, int64_t pb, const void* q, int64_t qb) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + static_cast<uintptr_t>(qb) && b < a + static_cast<uintptr_t>(pb);
+  };
+  const int64_t cb = M * h->N * 2;
+  if (overlap(C, cb, A_src, R * h->K) || overlap(C, cb, B, h->N * h->K) || overlap(C, cb, idx, M * 4))
+    return fail(SG_ERR_INVALID_ARG, "launch_gather: C overlaps an operand");
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return fail(SG_ERR_CUDA, "launch_gather: cudaGetDevice");
+  if (cur != h->device) return fail(SG_ERR_INVALID_ARG, "launch_gather: current device differs from the plan's");
+
+  sg::LaunchArgs a{};
+  a.mode = h->mode;
+  a.M = M;
+  a.N = h->N;
+  a.K = h->K;
+  a.A = A_src;
+  a.B = B;
+  a.a_scale = a_scale_src;
+  a.b_scale = b_scale;
+  a.C = C;
+  a.stream = s;
+  a.num_sms = h->num_sms;
+  a.status = h->status;
+  a.timeout_ns = h->timeout_ns;
+  a.skip_kstep = h->skip_kstep;
+  a.gather_idx = idx;
+  a.rows_src = R;
+  const sg_status_t r = sg::dense_launch_gather(a);
+  return r == SG_OK ? SG_OK : fail(r, "launch_gather: kernel launch");
+}
+
 sg_status_t scaled_gemm_quantize(int mode, int x_dtype, const void* X, int64_t R, int64_t C, void* Q,
                                  void* scale, sg_stream_t stream) {
   if (mode != SG_MODE_PTPC && mode != SG_MODE_BLOCKSCALE && mode != SG_MODE_MXFP8)

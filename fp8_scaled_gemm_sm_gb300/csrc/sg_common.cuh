@@ -32,6 +32,8 @@ struct GemmParams {
   const float* b_scale;      // ptpc [N]; blockscale [ceil(N/128)][K/128]
   int* status;               // device status word
   uint64_t timeout_ns;       // limit of every mbarrier wait
+  const int32_t* gather_idx; // gather-GEMM: source row of each output row [M] (else NULL)
+  int32_t rows_src;          // gather-GEMM: rows of the source A (and of a_scale)
 };
 
 // Persistent static schedule: CTA b takes tiles b, b + grid, b + 2*grid, ...

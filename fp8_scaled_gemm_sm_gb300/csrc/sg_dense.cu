@@ -52,7 +52,15 @@ struct DenseLayout {
   static_assert(kOffC % 1024 == 0, "store boxes need 512-byte alignment");
 };
 
-template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW>
+// GATHER (ptpc only): output row m reads source row p.gather_idx[m] of A (a
+// [rows_src][K] tensor map whose box is one row high) and its scale
+// a_scale[gather_idx[m]]; the 32 lanes of the producer warp each fetch four of
+// the tile's rows per stage with tile::gather4 (ROCm/aiter PR 6539, Technical
+// Details: the gather_kv_b_proj kernel gathers its A rows inside the GEMM's
+// pipeline).  An index outside [0, rows_src) -- and every row past M -- reads
+// source row 0 and gets scale 0, so no copy leaves the tensor and such a row's
+// output is zero (or clipped).
+template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW, bool GATHER = false>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
@@ -73,6 +81,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   static_assert(BN <= 256 && BN % 64 == 0, "BN");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
   static_assert(CLUSTER == 1 || CLUSTER == 2, "cluster size");
+  static_assert(!GATHER || MODE == kModePtpc, "the gather-GEMM is a ptpc GEMM");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -129,7 +138,63 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ---------------- TMA producer, A rows gathered by index (all 32 lanes) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+    int stage = 0, kstep = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    for (int tg = group; tg < num_group_tiles && ok; tg += ngroups) {
+      const TileCoord tc = coord(tg);
+      // this lane's rows of the tile: 4 lane .. 4 lane + 3
+      int32_t src[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int m = tc.mb * kBM + 4 * lane + q;
+        const int32_t v = m < p.M ? __ldg(p.gather_idx + m) : 0;
+        src[q] = (v >= 0 && v < p.rows_src) ? v : 0;
+      }
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty);
+        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        if (kstep != p.skip_kstep) {
+          if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), kTx);
+          __syncwarp();
+          tma_gather4(sA + stage * L::kAStage + lane * 4 * kRowBytes, &tmA, kb * kBK, src[0], src[1], src[2],
+                      src[3], full_bar(stage));
+          if (lane == 0) {
+            if constexpr (CLUSTER > 1)
+              tma_load_2d_multicast(sB + stage * L::kBStage + rank * kBRowsPerCta * kRowBytes, &tmB,
+                                    kb * kBK, tc.nb * BN + rank * kBRowsPerCta, full_bar(stage), kClusterMask);
+            else
+              tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN, full_bar(stage));
+            issued |= 1u << stage;
+            last_par[stage] = phase;
+          }
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (lane == 0) {
+      if (!ok) {  // loads still in flight must land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+      } else if (CLUSTER > 1) {
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
+      }
+    }
+  } else if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
@@ -245,7 +310,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           col_scale[i] = (n < p.N) ? p.b_scale[n] : 0.f;
         }
         const int row = m_start + lane;
-        row_scale = (row < p.M) ? p.a_scale[row] : 0.f;
+        if constexpr (GATHER) {
+          const int32_t v = row < p.M ? p.gather_idx[row] : -1;
+          row_scale = (v >= 0 && v < p.rows_src) ? p.a_scale[v] : 0.f;
+        } else {
+          row_scale = (row < p.M) ? p.a_scale[row] : 0.f;
+        }
         __syncwarp();
       }
       const bool ok = mbar_wait(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
@@ -531,10 +601,10 @@ constexpr int kDenseBN = 256;
 // it trades a stage for 8 epilogue warps (two per TMEM lane quarter).
 constexpr int kShortKBlocks = 4;
 
-template <int MODE, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW>
+template <int MODE, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW, bool GATHER = false>
 struct DenseKernel {
   using L = DenseLayout<kDenseBN, STAGES, EPI_WARPS, NBOX, BOXW>;
-  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX, CLUSTER, BOXW>;
+  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX, CLUSTER, BOXW, GATHER>;
   static constexpr int kBoxW = BOXW;
   static constexpr bool kPair = false;
   static constexpr int kThreads = 64 + 32 * EPI_WARPS;
@@ -565,6 +635,9 @@ template <int MODE>
 using LongK = PairKernel<MODE, kLongKStages, 8, 2>;
 template <int MODE>
 using ShortK = DenseKernel<MODE, kShortKStages, 8, 2, 2, 32>;
+// The gather-GEMM (ptpc): the short-K configuration with A gathered by index;
+// it serves any K (the gathered workload's K is 512).
+using GatherK = DenseKernel<kModePtpc, kShortKStages, 8, 2, 2, 32, true>;
 
 int dense_bk(int mode) { return mode == kModeBf16 ? 64 : 128; }
 
@@ -636,7 +709,9 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
 template <int MODE>
 cudaError_t prepare_dense() {
   cudaError_t e = LongK<MODE>::prepare();
-  return e == cudaSuccess ? ShortK<MODE>::prepare() : e;
+  if (e == cudaSuccess) e = ShortK<MODE>::prepare();
+  if (e == cudaSuccess && MODE == kModePtpc) e = GatherK::prepare();
+  return e;
 }
 
 }  // namespace
@@ -647,6 +722,32 @@ cudaError_t dense_prepare(int mode) {
 
 sg_status_t dense_launch(const LaunchArgs& a) {
   return a.mode == kModeBf16 ? launch_dense_impl<kModeBf16>(a) : launch_dense_impl<kModePtpc>(a);
+}
+
+sg_status_t dense_launch_gather(const LaunchArgs& a) {
+  CUtensorMap tmA, tmB;
+  // the source A [rows_src][K], one row per box (tile::gather4 fetches four of them)
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.rows_src, a.K, 128, 1,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kDenseBN / GatherK::kCluster,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return SG_ERR_CUDA;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(a.M);
+  p.N = static_cast<int32_t>(a.N);
+  p.K = static_cast<int32_t>(a.K);
+  p.m_blocks = static_cast<int32_t>((a.M + kBM - 1) / kBM);
+  p.n_blocks = static_cast<int32_t>((a.N + kDenseBN - 1) / kDenseBN);
+  p.k_blocks = static_cast<int32_t>((a.K + 127) / 128);
+  p.num_tiles = p.m_blocks * p.n_blocks;
+  p.skip_kstep = a.skip_kstep;
+  p.a_scale = static_cast<const float*>(a.a_scale);
+  p.b_scale = static_cast<const float*>(a.b_scale);
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  p.gather_idx = a.gather_idx;
+  p.rows_src = static_cast<int32_t>(a.rows_src);
+  return launch_with<GatherK>(a, tmA, tmB, p);
 }
 
 void dense_config(int mode, int64_t K, TileConfig* c) {

@@ -25,6 +25,8 @@ struct LaunchArgs {
   uint64_t timeout_ns;  // per-wait limit
   int32_t skip_kstep;   // watchdog tests: -1 = off
   void* workspace;      // the plan's device workspace (mxfp8: scale records), or NULL
+  const int32_t* gather_idx;  // gather-GEMM: idx [M] (else NULL); A is then the source [rows_src][K]
+  int64_t rows_src;
 };
 
 // Mode numbers as the launchers take them (equal to sg_mode_t).
@@ -61,6 +63,7 @@ sg_status_t quantize_launch(int mode, bool bf16, const void* X, int64_t R, int64
 
 cudaError_t dense_prepare(int mode);
 sg_status_t dense_launch(const LaunchArgs& a);
+sg_status_t dense_launch_gather(const LaunchArgs& a);  // ptpc, A rows gathered by a.gather_idx
 void dense_config(int mode, int64_t K, TileConfig* c);
 
 cudaError_t mxfp8_prepare();

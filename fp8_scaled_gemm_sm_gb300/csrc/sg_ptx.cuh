@@ -162,6 +162,18 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Indexed load (tile::gather4): rows y0..y3 of a 2D tensor, each `box` columns
+// from x (the tensor map's box is one row high), land in four consecutive rows at
+// dst, swizzled like a box load of those four rows.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+
 // Same load, multicast: the box lands at offset `dst` in the shared memory of
 // every CTA of the cluster named in `cta_mask`, and completes the transaction
 // count of the barrier at offset `bar` in each of them.

@@ -104,6 +104,21 @@ sg_status_t scaled_gemm_create(sg_handle_t* out, int mode, int64_t N, int64_t K,
 sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, const void* a_scale,
                                const void* b_scale, void* C, int64_t M, sg_stream_t stream);
 
+/* Gather-GEMM on a ptpc plan: output row i (0 <= i < M) is the ptpc GEMM row of
+ * source row idx[i] of A_src, scaled by a_scale_src[idx[i]] and b_scale[n]:
+ *   C[i][n] = bf16( (sum_k A_src[idx[i]][k] * B[n][k]) * a_scale_src[idx[i]] * b_scale[n] )
+ * A_src e4m3 [R][K] row-major, a_scale_src float[R], idx int32[M] (device
+ * pointers, 16-byte aligned, caller-owned); B, b_scale and C as for ptpc.  An index
+ * outside [0, R) names no row: that output row is zero (never read out of
+ * bounds).  The rows are gathered inside the GEMM's pipeline (TMA tile::gather4),
+ * not copied out first.  Shape rules as for ptpc, with 0 <= R < 2^31; R == 0 or
+ * K == 0 writes C = 0.  Returns SG_ERR_INVALID_ARG on a plan of another mode.
+ * Cited: ROCm/aiter PR 6539, Motivation and Technical Details (gather_kv_b_proj:
+ * the KV projection GEMM over rows gathered by index).                            */
+sg_status_t scaled_gemm_launch_gather(sg_handle_t h, const void* A_src, int64_t R, const int32_t* idx,
+                                      const void* B, const void* a_scale_src, const void* b_scale,
+                                      void* C, int64_t M, sg_stream_t stream);
+
 /* Release the plan.  NULL is accepted.  Must not race a launch on the same handle. */
 sg_status_t scaled_gemm_destroy(sg_handle_t h);
 

@@ -89,6 +89,13 @@ def test_noalloc_rejects_bad_arguments_on_the_host(lib):
     assert f(16, 32, 48, 64, 8, 16, 256, 256, None) == 3              # C misaligned
 
 
+def test_gather_rejects_a_null_handle_on_the_host(lib):
+    f = binding.lib().scaled_gemm_launch_gather
+    assert f(None, None, 16, None, None, None, None, None, 16, None) == 1   # NULL handle
+    # (checks on a plan -- wrong mode, bad R, NULL or misaligned operands -- need a
+    # device to create the plan and run in tests/test_gpu_gather.py)
+
+
 def test_quantize_rejects_bad_arguments_on_the_host(lib):
     f = binding.lib().scaled_gemm_quantize
     assert f(0, 0, None, 4, 128, None, None, None) == 1        # bf16 mode is not a quantisation mode
