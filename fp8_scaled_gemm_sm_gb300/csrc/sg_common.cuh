@@ -32,6 +32,7 @@ struct GemmParams {
   const float* b_scale;      // ptpc [N]; blockscale [ceil(N/128)][K/128]
   int* status;               // device status word
   uint64_t timeout_ns;       // limit of every mbarrier wait
+  const void* a_src;         // gather-GEMM: the source A [rows_src][K] e4m3 (else NULL)
   const int32_t* gather_idx; // gather-GEMM: source row of each output row [M] (else NULL)
   int32_t rows_src;          // gather-GEMM: rows of the source A (and of a_scale)
 };

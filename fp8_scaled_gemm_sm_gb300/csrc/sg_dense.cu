@@ -52,16 +52,19 @@ struct DenseLayout {
   static_assert(kOffC % 1024 == 0, "store boxes need 512-byte alignment");
 };
 
-// GATHER (ptpc only): output row m reads source row p.gather_idx[m] of A (a
-// [rows_src][K] tensor map whose box is one row high) and its scale
-// a_scale[gather_idx[m]]; the 32 lanes of the producer warp each fetch four of
-// the tile's rows per stage with tile::gather4 (ROCm/aiter PR 6539, Technical
-// Details: the gather_kv_b_proj kernel gathers its A rows inside the GEMM's
-// pipeline).  An index outside [0, rows_src) -- and every row past M -- reads
-// source row 0 and gets scale 0, so no copy leaves the tensor and such a row's
-// output is zero (or clipped).
+// GATHER (ptpc only): output row m reads source row p.gather_idx[m] of the source
+// A [rows_src][K] and its scale a_scale[gather_idx[m]] (ROCm/aiter PR 6539,
+// Technical Details: the gather_kv_b_proj kernel gathers its A rows inside the
+// GEMM's pipeline).  Two more warps (after the epilogue warps) copy the tile's
+// rows into the stage with 16-byte cp.async, eight lanes per row, writing the
+// 128-byte-swizzled layout the MMA reads, and arrive on full[s] as their copies
+// complete; B still comes by TMA.  (Gathering with TMA tile::gather4 took 33
+// copy operations per stage instead of 2 and ran 2.5x slower than the plain
+// GEMM, bound by the TMA unit.)  An index outside [0, rows_src) -- and every row
+// past M -- reads source row 0 and gets scale 0, so no copy leaves the source
+// and such a row's output is zero (or clipped).
 template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW, bool GATHER = false>
-__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS + (GATHER ? 64 : 0), 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -72,7 +75,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   constexpr int kKSteps = kBK / kUmmaK;
   constexpr uint32_t kIdesc =
       (MODE == kModeBf16) ? instr_desc(1, 1, kBM, BN) : instr_desc(0, 0, kBM, BN);
-  constexpr uint32_t kTx = L::kAStage + L::kBStage;
+  constexpr uint32_t kTx = GATHER ? L::kBStage : L::kAStage + L::kBStage;  // TMA bytes per stage
+  constexpr int kGatherThreads = GATHER ? 64 : 0;
   constexpr uint32_t kTmemCols = 512;
   constexpr int kAccStride = 256;
   constexpr int kColsPerWarp = BN * 4 / EPI_WARPS;
@@ -116,7 +120,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 1 + kGatherThreads);  // the producer's arm (+ each gather thread's copies)
       mbar_init(empty_bar(s), CLUSTER);  // one MMA commit from every CTA that reads the stage's B
     }
     for (int a = 0; a < 2; ++a) {
@@ -138,46 +142,48 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
 
-  if (warp == 0 && GATHER) {
-    // ---------------- TMA producer, A rows gathered by index (all 32 lanes) ----------------
-    if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-    }
+  if (GATHER && warp >= 2 + EPI_WARPS) {
+    // ---------------- A rows gathered by index (64 threads, cp.async) ----------------
+    const int t = (warp - 2 - EPI_WARPS) * 32 + lane;  // 0 .. 63
+    const int c = t & 7;                                // 16-byte chunk of the row's 128-byte K slice
+    const int r0 = t >> 3;                              // rows r0, r0 + 8, ..., r0 + 120 of the tile
+    // row r0 + 8 i, chunk c, at (r0 + 8 i) * 128 + ((c ^ r0) << 4): every row of
+    // this thread has swizzle phase r0
+    const uint32_t dst0 = r0 * kRowBytes + ((c ^ r0) << 4);
+    const uint8_t* A = static_cast<const uint8_t*>(p.a_src);
+    auto load_rows = [&](int tg, int32_t (&rows)[16]) {
+      const int mb = tg < num_group_tiles ? coord(tg).mb : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int m = mb * kBM + r0 + 8 * i;
+        const int32_t v = (tg < num_group_tiles && m < p.M) ? __ldg(p.gather_idx + m) : 0;
+        rows[i] = (v >= 0 && v < p.rows_src) ? v : 0;
+      }
+    };
+    int32_t next[16];
+    load_rows(group, next);
     int stage = 0, kstep = 0;
-    uint32_t phase = 0, issued = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int tg = group; tg < num_group_tiles && ok; tg += ngroups) {
-      const TileCoord tc = coord(tg);
-      // this lane's rows of the tile: 4 lane .. 4 lane + 3
-      int32_t src[4];
+      int32_t rows[16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int m = tc.mb * kBM + 4 * lane + q;
-        const int32_t v = m < p.M ? __ldg(p.gather_idx + m) : 0;
-        src[q] = (v >= 0 && v < p.rows_src) ? v : 0;
-      }
+      for (int i = 0; i < 16; ++i) rows[i] = next[i];
+      load_rows(tg + ngroups, next);  // one tile ahead
       for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty);
-        if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
           ok = false;
           break;
         }
         if (kstep != p.skip_kstep) {
-          if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), kTx);
-          __syncwarp();
-          tma_gather4(sA + stage * L::kAStage + lane * 4 * kRowBytes, &tmA, kb * kBK, src[0], src[1], src[2],
-                      src[3], full_bar(stage));
-          if (lane == 0) {
-            if constexpr (CLUSTER > 1)
-              tma_load_2d_multicast(sB + stage * L::kBStage + rank * kBRowsPerCta * kRowBytes, &tmB,
-                                    kb * kBK, tc.nb * BN + rank * kBRowsPerCta, full_bar(stage), kClusterMask);
-            else
-              tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN, full_bar(stage));
-            issued |= 1u << stage;
-            last_par[stage] = phase;
-          }
+          const int kofs = kb * kBK + 16 * c;
+          const uint32_t nbytes = kofs < p.K ? 16u : 0u;  // past K: zeros
+          const int koff = kofs < p.K ? kofs : 0;
+          const uint32_t dst = sA + stage * L::kAStage + dst0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            cp_async_16(dst + i * 8 * kRowBytes, A + static_cast<int64_t>(rows[i]) * p.K + koff, nbytes);
+          cp_async_arrive_noinc(full_bar(stage));
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -185,15 +191,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
         }
       }
     }
-    if (lane == 0) {
-      if (!ok) {  // loads still in flight must land before the CTA can exit
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
-      } else if (CLUSTER > 1) {
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
-      }
-    }
+    cp_async_wait_all();  // this thread's copies land before the CTA can exit
   } else if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -211,7 +209,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           }
           if (kstep != p.skip_kstep) {
             mbar_arrive_expect_tx(full_bar(stage), kTx);
-            tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
+            if constexpr (!GATHER)  // gathered A rows come from the gather warps
+              tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
             if constexpr (CLUSTER > 1)
               tma_load_2d_multicast(sB + stage * L::kBStage + rank * kBRowsPerCta * kRowBytes, &tmB,
                                     kb * kBK, tc.nb * BN + rank * kBRowsPerCta, full_bar(stage),
@@ -257,6 +256,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             ok = false;
             break;
           }
+          if constexpr (GATHER) fence_proxy_async_smem();  // the gather warps' cp.async data, for the MMA
           tc_fence_after();
           const uint32_t a0 = sA + stage * L::kAStage;
           const uint32_t b0 = sB + stage * L::kBStage;
@@ -607,7 +607,7 @@ struct DenseKernel {
   static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX, CLUSTER, BOXW, GATHER>;
   static constexpr int kBoxW = BOXW;
   static constexpr bool kPair = false;
-  static constexpr int kThreads = 64 + 32 * EPI_WARPS;
+  static constexpr int kThreads = 64 + 32 * EPI_WARPS + (GATHER ? 64 : 0);
   static constexpr int kCluster = CLUSTER;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
@@ -725,11 +725,8 @@ sg_status_t dense_launch(const LaunchArgs& a) {
 }
 
 sg_status_t dense_launch_gather(const LaunchArgs& a) {
-  CUtensorMap tmA, tmB;
-  // the source A [rows_src][K], one row per box (tile::gather4 fetches four of them)
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.rows_src, a.K, 128, 1,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kDenseBN / GatherK::kCluster,
+  CUtensorMap tmB;  // A is read by the kernel's gather warps, not by TMA
+  if (!encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kDenseBN / GatherK::kCluster,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return SG_ERR_CUDA;
   GemmParams p{};
@@ -745,9 +742,10 @@ sg_status_t dense_launch_gather(const LaunchArgs& a) {
   p.b_scale = static_cast<const float*>(a.b_scale);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
+  p.a_src = a.A;
   p.gather_idx = a.gather_idx;
   p.rows_src = static_cast<int32_t>(a.rows_src);
-  return launch_with<GatherK>(a, tmA, tmB, p);
+  return launch_with<GatherK>(a, tmB, tmB, p);  // (the A map argument is unused)
 }
 
 void dense_config(int mode, int64_t K, TileConfig* c) {

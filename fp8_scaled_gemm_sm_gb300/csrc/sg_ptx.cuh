@@ -162,17 +162,19 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// Indexed load (tile::gather4): rows y0..y3 of a 2D tensor, each `box` columns
-// from x (the tensor map's box is one row high), land in four consecutive rows at
-// dst, swizzled like a box load of those four rows.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
+// 16-byte asynchronous copy global -> shared (cp.async, L2 only); src_bytes = 0
+// writes 16 zero bytes without reading.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+
+// Arrive on the barrier once every cp.async this thread issued so far has
+// completed; the arrival is one of the barrier's expected arrivals.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Same load, multicast: the box lands at offset `dst` in the shared memory of
 // every CTA of the cluster named in `cta_mask`, and completes the transaction
