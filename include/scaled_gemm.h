@@ -88,7 +88,7 @@ typedef enum {
 /* Create a plan for one (mode, N, K) that serves any M <= M_max on `device`
  * (-1 = the current device).  The plan holds a 16-byte device status word, set
  * up here, that kernels write only when a wait times out; an mxfp8 plan also
- * allocates here its scale workspace, (ceil(M_max/128) + 2 ceil(N/224)) *
+ * allocates here its scale workspace, (ceil(M_max/128) + 8 ceil(N/224)) *
  * ceil(K/128) * 512 bytes of device memory.
  * On success *out receives the handle; on failure *out is set to NULL.
  * Cited: ROCm/mori PR 809, "Using it" (one instance serves one (n, k) and any M
