@@ -143,3 +143,27 @@ def test_mxfp8_shapes(gpu, M, N, K):
 )
 def test_blockscale_shapes(gpu, M, N, K):
     _run_full(gpu, synth.make_case("blockscale", M, N, K, seed=M + K, b_std=0.02), launches=8)
+
+
+def test_mxfp8_back_to_back_launches_on_one_plan(gpu):
+    # an mxfp8 plan rearranges each launch's scales in its workspace: two
+    # launches with different operands queued on one stream, with no host
+    # synchronisation between them, must each match their own oracle result
+    c1 = synth.make_case("mxfp8", 384, 448, 1024, seed=21, b_std=0.02)
+    c2 = synth.make_case("mxfp8", 384, 448, 1024, seed=22, b_std=0.02)
+    _, r1 = oracle.gemm("mxfp8", *c1.numpy(), want_r=False)
+    _, r2 = oracle.gemm("mxfp8", *c2.numpy(), want_r=False)
+    d1, d2 = gpu.DeviceCase(c1), gpu.DeviceCase(c2)
+    h = gpu.make_plan(c1)
+    try:
+        d1.poison()
+        d2.poison()
+        for _ in range(3):
+            d1.launch(h)
+            d2.launch(h)
+        torch.cuda.synchronize()
+        assert check(d1.c_bits(), r1)["ok"]
+        assert check(d2.c_bits(), r2)["ok"]
+        assert d1.canary_ok() and d2.canary_ok()
+    finally:
+        gpu.binding.scaled_gemm_destroy(h)
