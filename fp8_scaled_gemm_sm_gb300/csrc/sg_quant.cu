@@ -8,8 +8,9 @@
 //   ptpc / blockscale  s = amax / 448 (one fp32 IEEE division; s = 1 if amax = 0)
 //   mxfp8              e = the least integer with amax <= 448 * 2^e (0 if amax = 0),
 //                      code = clamp(e + 127, 0, 254), s = 2^(code - 127)
-//   q = e4m3(x / s): one fp32 IEEE division, then round to nearest even with
-//   saturation to +-448 (cvt.rn.satfinite).
+//   q = e4m3(x / s): the correctly rounded fp32 quotient (as one IEEE division
+//   gives it), then round to nearest even with saturation to +-448
+//   (cvt.rn.satfinite).
 //
 // One CTA of 256 threads per row (persistent over rows).  Thread t holds the
 // 8-element vectors t, t + 256, ... of its row in registers (16-byte loads), so
@@ -20,8 +21,8 @@
 // registers a thread), so loads stay in flight through the arithmetic.  The
 // algorithmic traffic is 2 (bf16) or 4 (fp32) bytes read and 1 byte written per
 // element, plus the scales; mxfp8 (a power-of-two scale: a multiply) runs near
-// that bound, ptpc and blockscale (an IEEE division per element) are partly
-// bound by instruction issue.
+// that bound; ptpc and blockscale form the quotient with a reciprocal and two
+// fma corrections instead of a division, which was most of their instructions.
 #include <cuda.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -116,14 +117,54 @@ __device__ __forceinline__ uint2 quant8_pow2(const float (&f)[8], float inv_s) {
   return cvt8(y);
 }
 
-// Eight codes of x / s: one IEEE fp32 division each, then e4m3.  (A reciprocal
-// multiply with a check for quotients near an e4m3 rounding midpoint was timed
-// as well: the check costs as many instructions as the division, and the
-// kernel is issue-bound there.)
-__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s) {
+// The correctly rounded quotient x / s without a division, by Markstein's method
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s), q = RN(x r), and
+// twice q <- RN(q + (x - q s) r), each remainder x - q s exact in one fma, the
+// second correction is RN(x / s) once r is correctly rounded and q within an ulp,
+// barring underflow.  Here it is taken only for 2^-60 <= s <= 2^60: every quotient
+// that can round to a nonzero e4m3 code (|x / s| >= 2^-11) then keeps its
+// remainders normal, and smaller quotients round to +-0 either way.  A zero x
+// would come out +0 from the corrections, so the sign of x is copied back (the
+// quotient's sign is x's: s > 0).  Two lanes per packed fp32x2 instruction.
+struct Recip {
+  uint64_t r2;    // (r, r)
+  uint64_t ns2;   // (-s, -s)
+  bool fast;      // s in [2^-60, 2^60]
+};
+
+__device__ __forceinline__ Recip make_recip(float s) {
+  const float r = __frcp_rn(s);
+  Recip q;
+  q.r2 = pack_f32x2(__float_as_uint(r), __float_as_uint(r));
+  q.ns2 = pack_f32x2(__float_as_uint(-s), __float_as_uint(-s));
+  q.fast = s >= 0x1p-60f && s <= 0x1p+60f;
+  return q;
+}
+
+// Eight codes of x / s: the quotient correctly rounded in fp32 (the IEEE division
+// where the scale is outside Markstein's range), then e4m3.
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, const Recip& rc) {
   float y[8];
+  if (rc.fast) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(f[i], s);
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a = __float_as_uint(f[2 * i]), b = __float_as_uint(f[2 * i + 1]);
+      const uint64_t x = pack_f32x2(a, b);
+      uint64_t q = mul_f32x2(x, rc.r2);
+      uint64_t e = fma_f32x2(q, rc.ns2, x);
+      q = fma_f32x2(e, rc.r2, q);
+      e = fma_f32x2(q, rc.ns2, x);
+      q = fma_f32x2(e, rc.r2, q);
+      float lo, hi;
+      unpack_f32x2(q, lo, hi);
+      y[2 * i] = __uint_as_float((__float_as_uint(lo) & 0x7FFFFFFFu) | (a & 0x80000000u));
+      y[2 * i + 1] = __uint_as_float((__float_as_uint(hi) & 0x7FFFFFFFu) | (b & 0x80000000u));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(f[i], s);
+  }
   return cvt8(y);
 }
 
@@ -188,10 +229,11 @@ __global__ void __launch_bounds__(kQThreads)
       for (int w = 0; w < kQThreads / 32; ++w) amax = fmaxf(amax, red[w]);
       const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
       if (tid == 0) static_cast<float*>(scale)[r] = s;
+      const Recip rc = make_recip(s);
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
         const int v = tid + i * kQThreads;
-        if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s);
+        if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s, rc);
       }
       __syncthreads();  // red[] is reused by the next row
     } else {
@@ -211,7 +253,7 @@ __global__ void __launch_bounds__(kQThreads)
           if (v < nvec && (v % kLanes) == 0) static_cast<float*>(scale)[static_cast<int64_t>(blk) * R + r] = s;
           if (v < nvec)
             *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) =
-                quant8(f[i], s);
+                quant8(f[i], s, make_recip(s));
         } else {
           int code = a > 0.f ? mx_exponent(a) + 127 : 127;
           code = code < 0 ? 0 : (code > 254 ? 254 : code);

@@ -97,6 +97,25 @@ def test_quantize_near_rounding_midpoints(lib, mode, bf16):
     assert np.array_equal(s.view(np.uint8), s_ref.view(np.uint8))
 
 
+@pytest.mark.parametrize("mode", ["ptpc", "blockscale"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantize_scales_on_both_sides_of_the_reciprocal_range(lib, mode, dtype):
+    # the kernel forms x / s with a reciprocal and fma corrections for scales in
+    # [2^-60, 2^60] and with a division outside; rows scaled from 2^-75 to 2^70
+    # put block and row scales on both sides of the bounds (and right at them)
+    g = torch.Generator("cpu")
+    g.manual_seed(31)
+    ex = torch.tensor([-75, -69, -60, -52, -51, 0, 51, 52, 60, 61, 66, 70] * 4, dtype=torch.float32)
+    x = torch.randn(ex.numel(), 2048, generator=g) * torch.exp2(ex)[:, None]
+    x[::3, ::5] *= 1e-6  # small values in the same rows and blocks
+    x = x.to(dtype)
+    q_ref, s_ref = oracle.quantize(mode, _host(x))
+    q, s = lib.quantize(mode, x.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(s.cpu().numpy().view(np.uint8), s_ref.view(np.uint8))
+
+
 def test_quantize_full_size_sampled_rows(lib):
     # the largest activation of the workloads, 32768 x 7168 bf16, every mode;
     # rows are independent, so the oracle checks a sample of them
