@@ -389,7 +389,7 @@ def kernel_name(mode, K):
     if mode == "mxfp8":
         return "mxfp8_pair_kernel"
     if mode == "blockscale":
-        return "blockscale_gemm_kernel"
+        return "blockscale_pair_kernel"
     short = (K + (63 if mode == "bf16" else 127)) // (64 if mode == "bf16" else 128) <= 4
     return ("dense_gemm_kernel<%s, short K>" if short else "dense_pair_kernel<%s>") % mode
 

@@ -11,25 +11,36 @@
 // "promotion" warps read it with tcgen05.ld, multiply by the two scales and add
 // it to an fp32 accumulator held in registers.
 //
-// Per CTA (one per SM, persistent over 128 x 256 output tiles: one N = 256 MMA
-// per K step, where 128-wide tiles ran 1.56x slower per FLOP; the tile covers
-// two B scale blocks, one per half):
+// Per CTA pair (two CTAs on neighbouring SMs, persistent over 256 x 256 output
+// tiles; the tile covers two B scale blocks, one per 128-column half):
 //   warpgroup 0 (120 registers a thread after setmaxnreg.dec):
-//     warp 0    TMA producer (A, B tiles into a 4-stage ring).
-//     warp 1    TMEM owner and MMA issuer: for K block j, wait full[s] and
-//               part_empty[p], 4 MMAs into partial buffer p (256 columns, 2
-//               buffers cycling across K blocks and tiles), commit empty[s] and
-//               part_full[p].
+//     warp 0    TMA producer, both CTAs: this CTA's 128 rows of A and its
+//               128-row half of B into a 6-stage ring (32 KB a stage); the
+//               bytes of both CTAs complete the even CTA's full[s].
+//     warp 1    TMEM owner (512 columns, allocated by the pair); in the even CTA
+//               the MMA issuer: for K block j, wait full[s] and part_empty[p], 4
+//               pair MMAs (tcgen05.mma.cta_group::2, 256 x 256 x 32) into
+//               partial buffer p (256 columns, 2 buffers cycling across K blocks
+//               and tiles; each CTA's TMEM holds its own 128 rows), then commit
+//               empty[s] and part_full[p] in both CTAs.
 //   warpgroups 1-2 (192 registers a thread after setmaxnreg.inc): promotion +
 //     epilogue, 2 warps per TMEM lane quarter, 128 columns (one B scale block)
 //     each; per K block wait part_full[p], read the buffer in two 64-column
-//     halves, release it after the second (tcgen05.fence::before_thread_sync +
-//     arrive part_empty[p]), acc += P * (sa * sb) with packed f32x2 FMAs; after
-//     the last block round to bf16 and store through shared memory and TMA.
-//     The 128 accumulators of a thread are why the register split exists.
+//     halves, hand it back after the second, acc += P * (sa * sb) with packed
+//     f32x2 FMAs; after the last block round to bf16 and store through shared
+//     memory and TMA.  The 128 accumulators of a thread are why the register
+//     split exists.
+// The hand-back of a partial is one arrive per promotion warp of both CTAs on
+// the even CTA's part_empty[p], after every lane's tcgen05.wait::ld, the
+// before-sync fence and __syncwarp, with relaxed semantics: it orders only the
+// TMEM reads, and a cluster-scope release would make every arrive wait for the
+// scale loads the warp has in flight (those run four K blocks ahead).
+// Against a single-CTA kernel on 128 x 256 tiles, the pair halves each SM's
+// operand bytes per FLOP; both are bound by the round trip of a partial
+// (commit, promotion reads, hand-back) through the two-deep buffer ring, so the
+// pair gains less than the halved operand traffic suggests.
 // The register split adds up to the launch allocation exactly (384 threads x 168
 // registers), so setmaxnreg.inc never waits for registers that cannot come.
-// The scales are loaded from global memory four K blocks ahead of their use.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -41,7 +52,6 @@ namespace sg {
 namespace {
 
 constexpr int kBsBN = 256;
-constexpr int kBsStages = 4;
 constexpr int kBsParts = 2;
 constexpr int kBsWarps = 8;                          // promotion warps
 constexpr int kBsThreads = 128 + 32 * kBsWarps;      // warpgroup 0 + two promotion warpgroups
@@ -53,21 +63,6 @@ static_assert(4 * kBsRegsCtl + 8 * kBsRegsPromo == 12 * kBsLaunchRegs,
               "the register split must equal the launch allocation");
 static_assert(kBsThreads * kBsLaunchRegs <= 65536, "launch allocation");
 
-struct BsLayout {
-  static constexpr int kAStage = kBM * kRowBytes;
-  static constexpr int kBStage = kBsBN * kRowBytes;
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kBsStages * kAStage;
-  static constexpr int kOffC = kOffB + kBsStages * kBStage;
-  static constexpr int kOffBar = kOffC + kBsWarps * 2 * kCBoxBytes;
-  static constexpr int kNumBars = 2 * kBsStages + 2 * kBsParts + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16 + 4 * kBsStages;
-  static constexpr int kDynSmem = kBytes + 1024;
-  static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "alignment");
-  static_assert(kDynSmem <= 232448, "shared memory");
-};
-
 __device__ __forceinline__ void regs_dec_ctl() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBsRegsCtl));
 }
@@ -75,16 +70,35 @@ __device__ __forceinline__ void regs_inc_promo() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBsRegsPromo));
 }
 
+constexpr int kBpStages = 6;
+constexpr int kBpBoxes = 2;  // C store boxes per promotion warp
+
+struct BpLayout {
+  static constexpr int kAStage = kBM * kRowBytes;
+  static constexpr int kBStage = (kBsBN / 2) * kRowBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kBpStages * kAStage;
+  static constexpr int kOffC = kOffB + kBpStages * kBStage;
+  static constexpr int kOffBar = kOffC + kBsWarps * kBpBoxes * kCBoxBytes;
+  static constexpr int kNumBars = 2 * kBpStages + 2 * kBsParts + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16 + 4 * kBpStages;
+  static constexpr int kDynSmem = kBytes + 1024;
+  static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "alignment");
+  static_assert(kDynSmem <= 232448, "shared memory");
+};
+
 __global__ void __launch_bounds__(kBsThreads, 1)
-    blockscale_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+    blockscale_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using L = BsLayout;
+  using L = BpLayout;
   constexpr int kBK = 128;
   constexpr int kKSteps = 4;
-  constexpr uint32_t kIdesc = instr_desc(0, 0, kBM, kBsBN);
-  constexpr uint32_t kTx = L::kAStage + L::kBStage;
+  constexpr uint32_t kIdesc = instr_desc(0, 0, 2 * kBM, kBsBN);
+  constexpr uint32_t kTxPair = 2 * (L::kAStage + L::kBStage);  // both CTAs' bytes
   constexpr uint32_t kTmemCols = 512;
+  constexpr uint16_t kBoth = 0x3;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -94,35 +108,48 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   const uint32_t sC = smem_addr(smem + L::kOffC);
   const uint32_t bar0 = smem_addr(smem + L::kOffBar);
   auto full_bar = [&](int s) { return bar0 + 8 * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8 * (kBsStages + s); };
-  auto pfull_bar = [&](int q) { return bar0 + 8 * (2 * kBsStages + q); };
-  auto pempty_bar = [&](int q) { return bar0 + 8 * (2 * kBsStages + kBsParts + q); };
-  const uint32_t drain_bar = bar0 + 8 * (2 * kBsStages + 2 * kBsParts);
+  auto empty_bar = [&](int s) { return bar0 + 8 * (kBpStages + s); };
+  auto pfull_bar = [&](int q) { return bar0 + 8 * (2 * kBpStages + q); };
+  auto pempty_bar = [&](int q) { return bar0 + 8 * (2 * kBpStages + kBsParts + q); };
+  const uint32_t drain_bar = bar0 + 8 * (2 * kBpStages + 2 * kBsParts);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   uint32_t* last_par = misc + 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_cta_rank());
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x());
+  const int npairs = static_cast<int>(num_clusters_x());
+  const int num_pair_tiles = ((p.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
+  auto coord = [&](int tp) {
+    TileCoord c;
+    const int mp = tp / p.n_blocks;
+    c.nb = tp - mp * p.n_blocks;
+    c.mb = 2 * mp + rank;  // this CTA's 128-row block
+    return c;
+  };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kBsStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < kBpStages; ++s) {
+      mbar_init(full_bar(s), 1);   // the leader's producer arms it for both CTAs' bytes
+      mbar_init(empty_bar(s), 1);  // one pair commit per round
     }
     for (int q = 0; q < kBsParts; ++q) {
       mbar_init(pfull_bar(q), 1);
-      mbar_init(pempty_bar(q), 32 * kBsWarps);
+      mbar_init(pempty_bar(q), 2 * kBsWarps);  // one elected lane per promotion warp of both CTAs
     }
     mbar_init(drain_bar, 1);
     misc[1] = 0;
     fence_mbarrier_init();
   }
-  if (warp == 1) {
-    tmem_alloc(smem_addr(&misc[0]), kTmemCols);
-    tmem_relinquish();
+  if (warp == 1) {  // one warp in each CTA of the pair allocates together
+    tmem_alloc_pair(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
@@ -130,46 +157,59 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   if (warp < 4) {
     regs_dec_ctl();
     if (warp == 0 && lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       const uint64_t keep_b = l2_policy_evict_last();
       int stage = 0, kstep = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const TileCoord tc = tile_coord(p, t);
+      for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
+        const TileCoord tc = coord(tp);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+          if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
             ok = false;
             break;
           }
           if (kstep != p.skip_kstep) {
-            mbar_arrive_expect_tx(full_bar(stage), kTx);
-            tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
-            tma_load_2d_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kBsBN, full_bar(stage), keep_b);
+            const uint32_t fb = map_to_cta(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
+            tma_load_2d_pair(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
+            tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK,
+                                  tc.nb * kBsBN + rank * (kBsBN / 2), fb, keep_b);
             issued |= 1u << stage;
             last_par[stage] = phase;
           }
-          if (++stage == kBsStages) {
+          if (++stage == kBpStages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < kBsStages; ++s)
-          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+        if (leader) {
+          for (int s = 0; s < kBpStages; ++s)
+            if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
+        } else {
+          // this CTA's loads complete on the leader's barrier: give them time to land
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 2000000ull) {
+          }
+        }
+      } else {
+        // every pair commit to this CTA's empty barriers must land before exit
+        for (int s = 0; s < kBpStages; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------- MMA issuer: one TMEM partial per K block ----------------
+    } else if (warp == 1 && lane == 0 && leader) {
+      // ---------------- pair MMA issuer: one TMEM partial per K block ----------------
       int stage = 0, part = 0;
       uint32_t phase = 0, ppar = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(pempty_bar(part), ppar ^ 1, wd, kWhereMmaTmemEmpty) ||
-              !mbar_wait(full_bar(stage), phase, wd, kWhereMmaFull)) {
+          if (!mbar_wait_cluster(pempty_bar(part), ppar ^ 1, wd, kWhereMmaTmemEmpty) ||
+              !mbar_wait_cluster(full_bar(stage), phase, wd, kWhereMmaFull)) {
             ok = false;
             break;
           }
@@ -179,10 +219,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           const uint32_t b0 = sB + stage * L::kBStage;
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k)
-            mma_f8f6f4(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k), kIdesc, k != 0);
-          mma_commit(empty_bar(stage));
-          mma_commit(pfull_bar(part));
-          if (++stage == kBsStages) {
+            mma_f8f6f4_pair(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k), kIdesc, k != 0);
+          mma_commit_pair(empty_bar(stage), kBoth);
+          mma_commit_pair(pfull_bar(part), kBoth);
+          if (++stage == kBpStages) {
             stage = 0;
             phase ^= 1;
           }
@@ -193,18 +233,18 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
       }
       if (!ok) {
-        mma_commit(drain_bar);
+        mma_commit_pair(drain_bar, 0x1);
         mbar_wait_drain(drain_bar, 0, 200000000ull);
       }
     }
   } else {
     regs_inc_promo();
-    // ---------------- promotion + epilogue ----------------
+    // ---------------- promotion + epilogue (both CTAs) ----------------
     const int ew = warp - 4;           // 0..7
     const int quarter = warp & 3;
     const int half = ew >> 2;          // which 128-column half of the tile (= B scale block)
     const int col0 = half * kBsCols;
-    const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
+    const uint32_t bufs = sC + ew * kBpBoxes * kCBoxBytes;
     const int kblocks = p.k_blocks;
     const int nsb = (p.N + 127) / 128;  // B scale blocks along N
     int part = 0;
@@ -222,8 +262,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     bool row_ok = false, col_ok = false;
     const float* sa_ptr = sa_base;
     const float* sb_ptr = sb_base;
-    auto tile_scale_ptrs = [&](int t) {
-      const TileCoord c = tile_coord(p, t);
+    const uint32_t release_bar0 = map_to_cta(pempty_bar(0), 0);  // the even CTA's part_empty[0]
+    auto tile_scale_ptrs = [&](int tp) {
+      const TileCoord c = coord(tp);
       const int row = c.mb * kBM + quarter * 32 + lane;
       const int sbr = 2 * c.nb + half;  // this warp's B scale block
       row_ok = row < p.M;
@@ -235,14 +276,14 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       a_out = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.M) : 0.f;
       b_out = col_ok ? __ldg(sb_ptr + kb) : 0.f;
     };
-    if (static_cast<int>(blockIdx.x) < p.num_tiles) {
-      tile_scale_ptrs(blockIdx.x);
+    if (pair < num_pair_tiles) {
+      tile_scale_ptrs(pair);
 #pragma unroll
       for (int d = 0; d < kScaleAhead; ++d)
         if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
     }
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-      const TileCoord tc = tile_coord(p, t);
+    for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
+      const TileCoord tc = coord(tp);
       const int m_start = tc.mb * kBM + quarter * 32;
       uint64_t acc[kBsCols / 2];
 #pragma unroll
@@ -255,7 +296,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
             const float sc = ring_a[d] * ring_b[d];
             const uint64_t s2 = pack_f32x2(__float_as_uint(sc), __float_as_uint(sc));
             if (kb + kScaleAhead < kblocks) load_scales(kb + kScaleAhead, ring_a[d], ring_b[d]);
-            ok = mbar_wait(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
+            ok = mbar_wait_cluster(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
             if (!__all_sync(0xffffffffu, ok)) {
               ok = false;
               break;
@@ -271,7 +312,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
               tmem_wait_ld();
               if (h == 1) {
                 tc_fence_before();
-                mbar_arrive(pempty_bar(part));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(release_bar0 + 8 * part);
               }
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -288,8 +330,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       }
       if (!ok) break;
       // the next tile's first scales load while this tile is stored
-      const int tn = t + static_cast<int>(gridDim.x);
-      if (tn < p.num_tiles) {
+      const int tn = tp + npairs;
+      if (tn < num_pair_tiles) {
         tile_scale_ptrs(tn);
 #pragma unroll
         for (int d = 0; d < kScaleAhead; ++d)
@@ -305,7 +347,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           unpack_f32x2(acc[16 * h + j], lo, hi);
           packed[j] = pack_bf16x2(lo, hi);
         }
-        store_box32(bufs, box, packed, &tmC, n_start + 32 * h, m_start, p.N, p.M, lane);
+        store_box32<kBpBoxes>(bufs, box, packed, &tmC, n_start + 32 * h, m_start, p.N, p.M, lane);
       }
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -315,24 +357,25 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal it or use its TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
 }  // namespace
 
 cudaError_t blockscale_prepare() {
-  return cudaFuncSetAttribute(blockscale_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              BsLayout::kDynSmem);
+  return cudaFuncSetAttribute(blockscale_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              BpLayout::kDynSmem);
 }
 
 sg_status_t blockscale_launch(const LaunchArgs& a) {
   CUtensorMap tmA, tmB, tmC;
   if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, 128, kBM,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kBsBN,
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kBsBN / 2,
                  CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols, kCBoxRows,
                  CU_TENSOR_MAP_SWIZZLE_64B))
@@ -350,18 +393,37 @@ sg_status_t blockscale_launch(const LaunchArgs& a) {
   p.b_scale = static_cast<const float*>(a.b_scale);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
-  blockscale_gemm_kernel<<<grid, kBsThreads, BsLayout::kDynSmem, a.stream>>>(tmA, tmB, tmC, p);
-  return launch_status();
+  const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
+  const int max_pairs = a.num_sms / 2;
+  const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(kBsThreads, 1, 1);
+  cfg.dynamicSmemBytes = BpLayout::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, blockscale_pair_kernel, tmA, tmB, tmC, p);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    cudaGetLastError();  // clear the non-sticky launch error
+    return SG_ERR_CUDA;
+  }
+  return SG_OK;
 }
 
 void blockscale_config(TileConfig* c) {
   c->bm = kBM;
   c->bn = kBsBN;
   c->bk = 128;
-  c->stages = kBsStages;
-  c->cluster = 1;
-  c->rows_per_group = kBM;
+  c->stages = kBpStages;
+  c->cluster = 2;
+  c->rows_per_group = 2 * kBM;
 }
 
 }  // namespace sg

@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       epilogue_tile<kColsPerWarp, kScaled, NBOX>(taddr, bufs, box, col_scale, row_scale, &tmC,
                                                  n_start, m_start, p.N, p.M, lane, [&]() {
                                                    tc_fence_before();
-                                                   mbar_arrive_cluster(release_bar);
+                                                   mbar_arrive_cluster_relaxed(release_bar);
                                                  });
     }
     if (lane == 0) bulk_wait_group<0>();

@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const uint32_t release_bar = map_to_cta(tempty_bar(acc), 0);
       auto release = [&]() {
         tc_fence_before();
-        mbar_arrive_cluster(release_bar);
+        mbar_arrive_cluster_relaxed(release_bar);
       };
       if (ew < 4)
         epilogue_tile<128, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N, p.M, lane,

@@ -223,6 +223,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Arrive on an mbarrier of a CTA of the cluster without releasing memory
+// operations: for a hand-back that orders only tcgen05 operations (a TMEM
+// buffer read with tcgen05.ld, then tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync), so the arrive does not wait for this
+// thread's outstanding global loads as a cluster-scope release would.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // Test-wait with acquire at cluster scope (for barriers that other CTAs arrive on).
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
   uint32_t done;
