@@ -139,6 +139,8 @@ def test_mxfp8_shapes(gpu, M, N, K):
         (128, 128, 256),
         (200, 272, 640),    # ragged M and N (N block partially outside)
         (256, 512, 2048),
+        (384, 896, 1152),   # the odd CTA of a pair tile wholly past M, its B half wholly past N; 9 K blocks
+        (2304, 2304, 384),  # 81 pair tiles on 76 pairs: second tiles, the partial ring's parity across tiles
     ],
 )
 def test_blockscale_shapes(gpu, M, N, K):
