@@ -37,19 +37,13 @@ struct GemmParams {
   int32_t rows_src;          // gather-GEMM: rows of the source A (and of a_scale)
 };
 
-// Persistent static schedule: CTA b takes tiles b, b + grid, b + 2*grid, ...
-// Tiles are numbered with the N block fastest, so the CTAs in flight at any
-// moment share a few A row panels and sweep all of B, which stays L2-resident.
+// Persistent static schedule: CTA pair (or CTA group) g takes tiles g, g + G,
+// g + 2G, ...  Tiles are numbered with the N block fastest, so the groups in
+// flight at any moment share a few A row panels and sweep all of B, which stays
+// L2-resident.  Each kernel maps a tile number to the 128-row block of its CTA.
 struct TileCoord {
-  int mb, nb;
+  int mb, nb;  // 128-row block of M, BN-column block of N
 };
-
-__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int t) {
-  TileCoord c;
-  c.mb = t / p.n_blocks;
-  c.nb = t - c.mb * p.n_blocks;
-  return c;
-}
 
 // Address of the 16-byte chunk `chunk` of row `row` in a 32-row store box of W
 // bf16 columns, laid out with the TMA swizzle of its row width: W = 32 (64-byte
