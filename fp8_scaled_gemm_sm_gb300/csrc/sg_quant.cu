@@ -12,11 +12,13 @@
 //   gives it), then round to nearest even with saturation to +-448
 //   (cvt.rn.satfinite).
 //
-// One CTA of 256 threads per row (persistent over rows).  Thread t holds the
-// 8-element vectors t, t + 256, ... of its row in registers (16-byte loads), so
-// the row is read once; the amax of a 128-element block lives in 16 consecutive
-// lanes and that of a 32-element block in 4, reduced with warp shuffles; a row
-// amax (ptpc) is reduced across the CTA.  While a row is processed, the raw
+// One CTA of 256 threads per row (persistent over rows).  Thread t holds
+// 8-element vectors of its row in registers (16-byte loads), so the row is read
+// once: for ptpc and mxfp8 the vectors t, t + 256, ... (the amax of a 32-element
+// block lives in 4 consecutive lanes, reduced with warp shuffles; a row amax is
+// reduced across the CTA); for blockscale groups of 4 consecutive vectors, so the
+// amax of a 128-element block lives in 4 consecutive lanes and the block's scale
+// and reciprocal are formed once per 32 elements.  While a row is processed, the raw
 // vectors of the CTA's next row are already being loaded (where they fit in 32
 // registers a thread), so loads stay in flight through the arithmetic.  The
 // algorithmic traffic is 2 (bf16) or 4 (fp32) bytes read and 1 byte written per
@@ -36,6 +38,7 @@ namespace {
 
 constexpr int kQThreads = 256;
 constexpr int kQMaxVecs = 16;  // vectors per thread: C <= 16 * 256 * 8 = 32768
+constexpr int kQGroup = 4;     // blockscale: consecutive vectors a thread takes in one block
 
 // Least integer e with amax <= 448 * 2^e, for finite amax > 0, by exact integer
 // comparison: amax = M * 2^q, 448 = 7 * 2^6, so e = t - 6 + q with t the least
@@ -176,13 +179,23 @@ __global__ void __launch_bounds__(kQThreads)
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int nvec = C / 8;
+  // Vector i of this thread in the row.  ptpc and mxfp8: vectors tid, tid + 256,
+  // ... (every load instruction of a warp reads 512 contiguous bytes).
+  // blockscale: groups of kVB consecutive vectors, so a thread's group lies in
+  // one 1x128 block (16 vectors), whose amax then needs 16 / kVB lanes, and the
+  // scale's division and reciprocal are taken once per group instead of once per
+  // vector.  Those two dominate the blockscale arithmetic; mxfp8's power-of-two
+  // scale is cheap, and there the strided loads of groups cost more than they save.
+  constexpr int kVB = (MODE == kModeBlockscale) ? (VPT < kQGroup ? VPT : kQGroup) : 1;
+  static_assert(VPT % kVB == 0, "whole groups per thread");
+  auto vidx = [&](int i) { return (i / kVB) * (kQThreads * kVB) + tid * kVB + (i % kVB); };
   // The next row's raw vectors are loaded while the current row is processed,
   // where they fit in 32 registers; otherwise each row is loaded when it starts.
   constexpr bool kPrefetch = VPT * (BF16 ? 4 : 8) <= 32;
   auto fetch = [&](Raw8<BF16> (&dst)[VPT], int rr) {
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int v = tid + i * kQThreads;
+      const int v = vidx(i);
       if (v < nvec && rr < R) load_raw8<BF16>(X, static_cast<int64_t>(rr) * C + 8 * static_cast<int64_t>(v), dst[i]);
     }
   };
@@ -202,7 +215,7 @@ __global__ void __launch_bounds__(kQThreads)
     } else {
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
-        const int v = tid + i * kQThreads;
+        const int v = vidx(i);
         Raw8<BF16> raw;
         if (v < nvec) load_raw8<BF16>(X, row + 8 * static_cast<int64_t>(v), raw);
         unpack8<BF16>(raw, f[i]);
@@ -212,7 +225,7 @@ __global__ void __launch_bounds__(kQThreads)
     // the block size) hold zeros
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
-      if (tid + i * kQThreads >= nvec)
+      if (vidx(i) >= nvec)
 #pragma unroll
         for (int j = 0; j < 8; ++j) f[i][j] = 0.f;
     if constexpr (MODE == kModePtpc) {
@@ -232,37 +245,56 @@ __global__ void __launch_bounds__(kQThreads)
       const Recip rc = make_recip(s);
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
-        const int v = tid + i * kQThreads;
+        const int v = vidx(i);
         if (v < nvec) *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) = quant8(f[i], s, rc);
       }
       __syncthreads();  // red[] is reused by the next row
     } else {
-      // a block is 16 (1x128) or 4 (1x32) consecutive vectors = lanes of one warp
-      constexpr int kLanes = MODE == kModeBlockscale ? 16 : 4;
+      // a block is kBV consecutive vectors: the groups of kLanes consecutive lanes
+      // of one warp (C is a multiple of the block, so a group is wholly inside
+      // or wholly past the row)
+      constexpr int kBV = MODE == kModeBlockscale ? 16 : 4;
+      constexpr int kLanes = kBV / kVB;
+      static_assert(kBV % kVB == 0, "a group inside one block");
 #pragma unroll
-      for (int i = 0; i < VPT; ++i) {
+      for (int g = 0; g < VPT / kVB; ++g) {
         float a = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[i][j]));
+        for (int j = 0; j < kVB; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[g * kVB + j][e]));
 #pragma unroll
         for (int o = kLanes / 2; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        const int v = tid + i * kQThreads;
-        const int blk = v / kLanes;
+        const int v0 = vidx(g * kVB);
+        const bool live = v0 < nvec;
+        const int blk = v0 / kBV;
+        uint2 codes[kVB];
         if constexpr (MODE == kModeBlockscale) {
           const float s = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
-          if (v < nvec && (v % kLanes) == 0) static_cast<float*>(scale)[static_cast<int64_t>(blk) * R + r] = s;
-          if (v < nvec)
-            *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) =
-                quant8(f[i], s, make_recip(s));
+          if (live && (v0 % kBV) == 0) static_cast<float*>(scale)[static_cast<int64_t>(blk) * R + r] = s;
+          const Recip rc = make_recip(s);
+#pragma unroll
+          for (int j = 0; j < kVB; ++j) codes[j] = quant8(f[g * kVB + j], s, rc);
         } else {
           int code = a > 0.f ? mx_exponent(a) + 127 : 127;
           code = code < 0 ? 0 : (code > 254 ? 254 : code);
-          if (v < nvec && (v % kLanes) == 0)
+          if (live && (v0 % kBV) == 0)
             static_cast<uint8_t*>(scale)[static_cast<int64_t>(blk) * R + r] = static_cast<uint8_t>(code);
           // 1/s = 2^(127 - code), code in [0, 254]: representable (normal or 2^-127)
-          if (v < nvec)
-            *reinterpret_cast<uint2*>(Q + row + 8 * static_cast<int64_t>(v)) =
-                quant8_pow2(f[i], exp2_code(254 - code));
+          const float inv_s = exp2_code(254 - code);
+#pragma unroll
+          for (int j = 0; j < kVB; ++j) codes[j] = quant8_pow2(f[g * kVB + j], inv_s);
+        }
+        if (live) {
+          uint8_t* dst = Q + row + 8 * static_cast<int64_t>(v0);  // 8 kVB-byte aligned
+          if constexpr (kVB == 1) {
+            *reinterpret_cast<uint2*>(dst) = codes[0];
+          } else {
+#pragma unroll
+            for (int j = 0; j < kVB; j += 2)
+              *reinterpret_cast<uint4*>(dst + 8 * j) =
+                  make_uint4(codes[j].x, codes[j].y, codes[j + 1].x, codes[j + 1].y);
+          }
         }
       }
     }
