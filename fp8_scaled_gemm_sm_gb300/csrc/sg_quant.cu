@@ -171,8 +171,18 @@ __device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, const Reci
   return cvt8(y);
 }
 
+// Resident CTAs a launch sizes its registers for (0: the compiler's choice).
+// mxfp8 on bf16 rows of 4 vectors a thread (4097 to 8192 elements) fits four
+// CTAs an SM (64 registers, no spills) where the compiler alone takes three;
+// an explicit bound elsewhere either spills or, at one CTA, lets ptpc and
+// blockscale grow past three CTAs' registers.
 template <int MODE, bool BF16, int VPT>
-__global__ void __launch_bounds__(kQThreads)
+constexpr int q_min_ctas() {
+  return (MODE == kModeMxfp8 && BF16 && VPT == 4) ? 4 : 0;
+}
+
+template <int MODE, bool BF16, int VPT>
+__global__ void __launch_bounds__(kQThreads, (q_min_ctas<MODE, BF16, VPT>()))
     quantize_kernel(const void* __restrict__ X, uint8_t* __restrict__ Q, void* __restrict__ scale,
                     int R, int C) {
   __shared__ float red[kQThreads / 32];
