@@ -33,6 +33,7 @@ SIGNATURES = {
     "scaled_gemm_destroy": (_int, [_vp]),
     "scaled_gemm_status_string": (ctypes.c_char_p, [_int]),
     "scaled_gemm_get_config": (_int, [_vp] + [ctypes.POINTER(_int)] * 5),
+    "scaled_gemm_set_tile": (_int, [_vp, _int]),
     "scaled_gemm_debug_status": (_int, [_vp, _vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "scaled_gemm_set_debug": (_int, [_vp, _i64, _i64]),
     "scaled_gemm_launch_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
@@ -153,6 +154,10 @@ def scaled_gemm_debug_status(h, stream=0):
     code, where = ctypes.c_int32(), ctypes.c_int32()
     _check(lib().scaled_gemm_debug_status(h, stream or None, ctypes.byref(code), ctypes.byref(where)), "scaled_gemm_debug_status")
     return code.value, where.value
+
+
+def scaled_gemm_set_tile(h, bn=0):
+    _check(lib().scaled_gemm_set_tile(h, int(bn)), "scaled_gemm_set_tile")
 
 
 def scaled_gemm_set_debug(h, timeout_ns=0, skip_kstep=-1):

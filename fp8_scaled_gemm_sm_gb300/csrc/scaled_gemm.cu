@@ -24,6 +24,7 @@ struct sg_gemm {
   void* workspace;  // device; mxfp8: the scale records of one launch (else NULL)
   uint64_t timeout_ns;
   int32_t skip_kstep;
+  int tile_bn;  // output-tile width pinned by scaled_gemm_set_tile, or 0
 };
 
 namespace {
@@ -182,6 +183,7 @@ sg_status_t scaled_gemm_create(sg_handle_t* out, int mode, int64_t N, int64_t K,
   h->workspace = workspace;
   h->timeout_ns = kDefaultTimeoutNs;
   h->skip_kstep = -1;
+  h->tile_bn = 0;
   *out = h;
   return SG_OK;
 }
@@ -207,7 +209,7 @@ sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int
   switch (h->mode) {
     case SG_MODE_BF16:
     case SG_MODE_PTPC: sg::dense_config(h->mode, h->K, &c); break;
-    case SG_MODE_MXFP8: sg::mxfp8_config(&c); break;
+    case SG_MODE_MXFP8: sg::mxfp8_config(h->M_max, h->N, h->num_sms, h->tile_bn, &c); break;
     case SG_MODE_BLOCKSCALE: sg::blockscale_config(&c); break;
   }
   if (bm) *bm = c.bm;
@@ -219,6 +221,25 @@ sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int
     const int64_t max_groups = h->num_sms / c.cluster;
     *grid = static_cast<int>((groups < max_groups ? groups : max_groups) * c.cluster);
   }
+  return SG_OK;
+}
+
+sg_status_t scaled_gemm_set_tile(sg_handle_t h, int bn) {
+  if (!h) return fail(SG_ERR_INVALID_ARG, "set_tile: NULL handle");
+  if (bn == 0) {
+    h->tile_bn = 0;
+    return SG_OK;
+  }
+  sg::TileConfig c{};
+  bool ok = false;
+  switch (h->mode) {
+    case SG_MODE_MXFP8: ok = sg::mxfp8_tile_ok(bn); break;
+    case SG_MODE_BF16:
+    case SG_MODE_PTPC: sg::dense_config(h->mode, h->K, &c); ok = bn == c.bn; break;
+    case SG_MODE_BLOCKSCALE: sg::blockscale_config(&c); ok = bn == c.bn; break;
+  }
+  if (!ok) return fail(SG_ERR_INVALID_ARG, "set_tile: a width this mode does not have");
+  h->tile_bn = bn;
   return SG_OK;
 }
 
@@ -291,6 +312,7 @@ sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, cons
   a.status = h->status;
   a.timeout_ns = h->timeout_ns;
   a.skip_kstep = h->skip_kstep;
+  a.tile_bn = h->tile_bn;
   a.workspace = h->workspace;
   sg_status_t r = SG_ERR_INVALID_ARG;
   switch (h->mode) {
@@ -349,6 +371,7 @@ sg_status_t scaled_gemm_launch_gather(sg_handle_t h, const void* A_src, int64_t 
   a.status = h->status;
   a.timeout_ns = h->timeout_ns;
   a.skip_kstep = h->skip_kstep;
+  a.tile_bn = h->tile_bn;
   a.gather_idx = idx;
   a.rows_src = R;
   const sg_status_t r = sg::dense_launch_gather(a);

@@ -27,6 +27,7 @@ struct LaunchArgs {
   void* workspace;      // the plan's device workspace (mxfp8: scale records), or NULL
   const int32_t* gather_idx;  // gather-GEMM: idx [M] (else NULL); A is then the source [rows_src][K]
   int64_t rows_src;
+  int tile_bn;          // output-tile width pinned on the plan, or 0: chosen per launch
 };
 
 // Mode numbers as the launchers take them (equal to sg_mode_t).
@@ -69,7 +70,8 @@ void dense_config(int mode, int64_t K, TileConfig* c);
 cudaError_t mxfp8_prepare();
 size_t mxfp8_workspace_bytes(int64_t M_max, int64_t N, int64_t K);  // scale records
 sg_status_t mxfp8_launch(const LaunchArgs& a);
-void mxfp8_config(TileConfig* c);
+void mxfp8_config(int64_t M, int64_t N, int num_sms, int tile_bn, TileConfig* c);
+bool mxfp8_tile_ok(int bn);  // a width the mxfp8 kernels have
 
 cudaError_t blockscale_prepare();
 sg_status_t blockscale_launch(const LaunchArgs& a);

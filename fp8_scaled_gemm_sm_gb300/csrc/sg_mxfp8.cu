@@ -24,7 +24,7 @@
 //    faster).  Missing rows and K blocks are 0 (their A / B values are
 //    zero-filled by TMA).  It reads (M + N) K / 32 bytes and writes (M + 4 N) K / 32.
 //
-// 2. mxfp8_pair_kernel: two CTAs on neighbouring SMs (a cluster of 2) compute
+// 2. mxfp8_pair_kernel<224>: two CTAs on neighbouring SMs (a cluster of 2) compute
 //    one 256 x 224 output tile with the pair MMA.  Each CTA stages its own 128
 //    rows of A and 112 of the tile's 224 rows of B, so per SM the shared memory
 //    written by TMA and read by the MMA per FLOP is that of a 128 x 448 tile; a
@@ -36,6 +36,10 @@
 //    completes the even CTA's full[s].  (Regrouping the raw scales in a warp of
 //    each CTA instead put a per-stage cross-CTA release on the critical path and
 //    ran 2x slower.)
+//
+//    mxfp8_pair_kernel<128> is the same kernel on 256 x 128 tiles, for launches
+//    where 224-wide tiles would leave pairs of SMs idle (small M); its B scales
+//    fit one 128-row chunk and travel in 512-byte records like A's.
 //
 // Per CTA of the pair kernel, persistent over pair tiles (N block fastest):
 //   warp 0     TMA producer: A rows, B half and scale records into stage s.
@@ -62,42 +66,65 @@ namespace sg {
 
 namespace {
 
-constexpr int kMxBN = 224;                 // N of a pair tile (and of each CTA's accumulator)
-constexpr int kMxBHalf = kMxBN / 2;        // B rows each CTA stages
-constexpr int kMxStages = 5;
+constexpr int kMxBN = 224;                 // N of a wide pair tile (and of each CTA's accumulator)
+constexpr int kMxBNarrow = 128;            // N of a narrow pair tile
 constexpr int kMxEpiWarps = 8;
 constexpr int kMxThreads = 64 + 32 * kMxEpiWarps;
 constexpr int kRec = 512;                  // bytes of one scale record (32 rows x 16 B)
 
+// The two tile widths.  Wide (224): B's scales span two 128-row chunks, held in
+// one 4 KB record per tile and K step (one 128x256b copy); 5 stages.  Narrow
+// (128): one chunk, held like A's in a 512-byte record (one 32x128b.warpx4 copy);
+// B stages are half as large, so 6 stages fit.
+template <int BN>
+struct MxTile {
+  static_assert(BN == kMxBN || BN == kMxBNarrow, "tile width");
+  static constexpr bool kWide = BN == kMxBN;
+  static constexpr int kBHalf = BN / 2;    // B rows each CTA stages
+  static constexpr int kStages = kWide ? 5 : 6;
+  static constexpr int kSfB = kWide ? 8 * kRec : kRec;
+  static constexpr int kSfBRows = kSfB / kRec;  // 512-byte record rows per B record
+};
+
+template <int BN>
 struct MxLayout {
+  using T = MxTile<BN>;
+  static constexpr int kStages = T::kStages;
   static constexpr int kAStage = kBM * kRowBytes;        // 16 KB
-  static constexpr int kBStage = kMxBHalf * kRowBytes;   // 14 KB
+  static constexpr int kBStage = T::kBHalf * kRowBytes;  // 14 KB (wide), 8 KB (narrow)
   static constexpr int kSfA = kRec;                      // A's record
-  static constexpr int kSfB = 8 * kRec;                  // B's record: 128 lanes x 32 B
+  static constexpr int kSfB = T::kSfB;                   // B's record
   static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + kMxStages * kAStage;
-  static constexpr int kOffC = kOffB + kMxStages * kBStage;
+  static constexpr int kOffB = kOffA + kStages * kAStage;
+  static constexpr int kOffC = kOffB + kStages * kBStage;
   static constexpr int kOffSfA = kOffC + kMxEpiWarps * 2 * kCBoxBytes;
-  static constexpr int kOffSfB = kOffSfA + kMxStages * kSfA;
-  static constexpr int kOffBar = kOffSfB + kMxStages * kSfB;
-  static constexpr int kNumBars = 2 * kMxStages + 5;
+  static constexpr int kOffSfB = kOffSfA + kStages * kSfA;
+  static constexpr int kOffBar = kOffSfB + kStages * kSfB;
+  static constexpr int kNumBars = 2 * kStages + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16 + 4 * kMxStages;
+  static constexpr int kBytes = kOffMisc + 16 + 4 * kStages;
   static constexpr int kDynSmem = kBytes + 1024;
   static_assert(kOffB % 1024 == 0 && kBStage % 1024 == 0 && kOffC % 1024 == 0, "alignment");
   static_assert(kOffSfA % 128 == 0 && kOffSfB % 128 == 0, "TMA / scale-record alignment");
   static_assert(kDynSmem <= 232448, "shared memory");
 };
 
-// TMEM columns: accumulators at 0 and 256 (224 wide each); per-stage scale
-// factors (A 4 columns, B 8) in the gaps [224, 256) and [480, 512).
+// TMEM columns.  Wide: accumulators at 0 and 256 (224 wide each); per-stage scale
+// factors (A 4 columns, B 8) in the gaps [224, 256) and [480, 512).  Narrow:
+// accumulators at 0 and 256 (128 wide each); stage s's scale factors (A 4
+// columns, B 4) at 128 + 8 s.
+template <int BN>
 __device__ __forceinline__ uint32_t sf_col_a(int s) {
-  return s == 0 ? 224 : s == 1 ? 236 : s == 2 ? 480 : s == 3 ? 492 : 248;
+  if constexpr (BN == kMxBN) return s == 0 ? 224 : s == 1 ? 236 : s == 2 ? 480 : s == 3 ? 492 : 248;
+  else return 128 + 8 * s;
 }
+template <int BN>
 __device__ __forceinline__ uint32_t sf_col_b(int s) {
-  return s == 0 ? 228 : s == 1 ? 240 : s == 2 ? 484 : s == 3 ? 496 : 504;
+  if constexpr (BN == kMxBN) return s == 0 ? 228 : s == 1 ? 240 : s == 2 ? 484 : s == 3 ? 496 : 504;
+  else return 132 + 8 * s;
 }
-static_assert(kMxStages <= 5, "TMEM has scale-factor room for 5 stages");
+static_assert(MxTile<kMxBN>::kStages <= 5, "TMEM has scale-factor room for 5 wide stages");
+static_assert(128 + 8 * MxTile<kMxBNarrow>::kStages <= 256, "narrow scale factors below the second accumulator");
 
 // A 32-row x 16-byte record in shared memory as 8-row x 16-byte core matrices:
 // row r at (r / 8) * 128 + (r % 8) * 16 = 16 r.
@@ -108,15 +135,19 @@ __device__ __forceinline__ void tmem_cp_pair_32x128b_x4(uint32_t taddr, uint64_t
 }
 
 // Records of the workspace, in 512-byte rows.  A: record (mc, ks) is row
-// mc * k_steps + ks.  B: the record of (N tile nt, step ks) is 8 rows from row
-// (nt * k_steps + ks) * 8: the 128-lane x 32-byte source of one
+// mc * k_steps + ks.  B, wide tiles: the record of (N tile nt, step ks) is 8 rows
+// from row (nt * k_steps + ks) * 8: the 128-lane x 32-byte source of one
 // tcgen05.cp.128x256b, lane l holding its 16-byte words for the tile's 128-row
 // chunks 0 and 1 at (l / 8) * 256 + j * 128 + (l % 8) * 16 (every 32-lane quarter
-// repeats the same rows, as the MMA wants them in every quarter).
+// repeats the same rows, as the MMA wants them in every quarter).  B, narrow
+// tiles: row nt * k_steps + ks, laid out as A's records.
 struct RecGeom {
   int M, N, kblk, k_steps, m_chunks, n_tiles;
+  bool wide;  // B records for 224-row tiles (else 128-row tiles)
   __host__ __device__ int64_t a_records() const { return static_cast<int64_t>(m_chunks) * k_steps; }
-  __host__ __device__ int64_t b_rows() const { return static_cast<int64_t>(n_tiles) * k_steps * 8; }
+  __host__ __device__ int64_t b_rows() const {
+    return static_cast<int64_t>(n_tiles) * k_steps * (wide ? 8 : 1);
+  }
 };
 
 // One thread per 32-bit word: the four K-block scales of one row.  In an A record
@@ -145,7 +176,7 @@ __global__ void __launch_bounds__(256)
       src = sa;
       pitch = g.M;
       pos = rec * 128 + r * 4 + c;
-    } else {
+    } else if (g.wide) {
       const int64_t wi = i - words_a;
       const int64_t q = wi >> 10;  // (nt, ks) record: 1024 words
       const int t = static_cast<int>(wi & 1023);
@@ -158,6 +189,18 @@ __global__ void __launch_bounds__(256)
       src = sb;
       pitch = g.N;
       pos = q * 1024 + (l >> 3) * 64 + j * 32 + (l & 7) * 4 + c;
+    } else {
+      const int64_t wi = i - words_a;
+      const int64_t q = wi >> 7;  // (nt, ks) record: 128 words, as A's
+      const int t = static_cast<int>(wi & 127);
+      const int r = t & 31, c = t >> 5;
+      const int nt = static_cast<int>(q / g.k_steps);
+      ks = static_cast<int>(q - static_cast<int64_t>(nt) * g.k_steps);
+      row = nt * kMxBNarrow + 32 * c + r;
+      valid = row < g.N;
+      src = sb;
+      pitch = g.N;
+      pos = q * 128 + r * 4 + c;
     }
     uint32_t w = 0;
     if (valid) {
@@ -175,11 +218,14 @@ __device__ __forceinline__ void tmem_cp_pair_128x256b(uint32_t taddr, uint64_t s
   asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kMxThreads, 1)
     mxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmRA, const __grid_constant__ CUtensorMap tmRB,
                       const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using L = MxLayout;
+  using L = MxLayout<BN>;
+  using T = MxTile<BN>;
+  constexpr int kMxStages = L::kStages;
   constexpr int kBK = 128;
   constexpr int kKSteps = 4;
   constexpr uint32_t kTxPair = 2 * (L::kAStage + L::kBStage + L::kSfA + L::kSfB);  // both CTAs' bytes
@@ -265,11 +311,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const uint32_t fb = map_to_cta(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
             tma_load_2d_pair(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
-            tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * kMxBN + rank * kMxBHalf, fb,
+            tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN + rank * T::kBHalf, fb,
                                   keep_b);
             // records past the last M chunk read as zeros
             tma_load_2d_pair(sSfA + stage * L::kSfA, &tmRA, 0, tc.mb * p.k_blocks + kb, fb);
-            tma_load_2d_pair(sSfB + stage * L::kSfB, &tmRB, 0, (tc.nb * p.k_blocks + kb) * 8, fb);
+            tma_load_2d_pair(sSfB + stage * L::kSfB, &tmRB, 0, (tc.nb * p.k_blocks + kb) * T::kSfBRows, fb);
             issued |= 1u << stage;
             last_par[stage] = phase;
           }
@@ -316,16 +362,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t tsa = tmem_base + sf_col_a(stage);
-          const uint32_t tsb = tmem_base + sf_col_b(stage);
+          const uint32_t tsa = tmem_base + sf_col_a<BN>(stage);
+          const uint32_t tsb = tmem_base + sf_col_b<BN>(stage);
           tmem_cp_pair_32x128b_x4(tsa, rec_desc(sSfA + stage * L::kSfA));
-          tmem_cp_pair_128x256b(tsb, smem_desc(sSfB + stage * L::kSfB, 128, 256, 0));
+          if constexpr (T::kWide)
+            tmem_cp_pair_128x256b(tsb, smem_desc(sSfB + stage * L::kSfB, 128, 256, 0));
+          else
+            tmem_cp_pair_32x128b_x4(tsb, rec_desc(sSfB + stage * L::kSfB));
           const uint32_t a0 = sA + stage * L::kAStage;
           const uint32_t b0 = sB + stage * L::kBStage;
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k) {
             mma_mxf8_pair(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k),
-                          instr_desc_mx(2 * kBM, kMxBN, k, k), tsa, tsb, (kb | k) != 0);
+                          instr_desc_mx(2 * kBM, BN, k, k), tsa, tsb, (kb | k) != 0);
           }
           mma_commit_pair(empty_bar(stage), kBoth);
           if (++stage == kMxStages) {
@@ -345,7 +394,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // ---------------- epilogue (both CTAs) ----------------
     const int ew = warp - 2;                 // 0 .. 7
     const int quarter = warp & 3;            // TMEM lanes this warp may access
-    const int col0 = ew < 4 ? 0 : 128;       // columns 0-127 or 128-223 of the tile
+    // wide: columns 0-127 or 128-223 of the tile; narrow: 0-63 or 64-127
+    constexpr int kColsLo = T::kWide ? 128 : 64;
+    constexpr int kColsHi = BN - kColsLo;
+    const int col0 = ew < 4 ? 0 : kColsLo;
     const uint32_t bufs = sC + ew * 2 * kCBoxBytes;
     int it = 0;
     uint32_t box = 0;
@@ -354,7 +406,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const int acc = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
       const int m_start = tc.mb * kBM + quarter * 32;
-      const int n_start = tc.nb * kMxBN + col0;
+      const int n_start = tc.nb * BN + col0;
       const bool ok = mbar_wait_cluster(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -366,11 +418,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         mbar_arrive_cluster_relaxed(release_bar);
       };
       if (ew < 4)
-        epilogue_tile<128, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N, p.M, lane,
-                                  release);
+        epilogue_tile<kColsLo, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N, p.M, lane,
+                                      release);
       else
-        epilogue_tile<kMxBN - 128, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N,
-                                          p.M, lane, release);
+        epilogue_tile<kColsHi, false>(taddr, bufs, box, nullptr, 0.f, &tmC, n_start, m_start, p.N, p.M, lane,
+                                      release);
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
@@ -386,33 +438,111 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
-RecGeom rec_geom(int64_t M, int64_t N, int64_t K) {
+RecGeom rec_geom(int64_t M, int64_t N, int64_t K, int bn) {
   RecGeom g;
   g.M = static_cast<int>(M);
   g.N = static_cast<int>(N);
   g.kblk = static_cast<int>(K / 32);
   g.k_steps = static_cast<int>((K + 127) / 128);
   g.m_chunks = static_cast<int>((M + kBM - 1) / kBM);
-  g.n_tiles = static_cast<int>((N + kMxBN - 1) / kMxBN);
+  g.n_tiles = static_cast<int>((N + bn - 1) / bn);
+  g.wide = bn == kMxBN;
   return g;
+}
+
+// Tile width of a launch: the one with the smaller estimate of waves of pair
+// tiles x tile width x cost of a column.  A narrow tile's column costs more (it
+// stages A once per 128 columns instead of per 224, and copies two scale records
+// per 128 columns): 1.32-1.42x, from timings at N = 7168, K = 1792 and M = 2048
+// to 8192.  Narrow tiles win where wide ones leave pairs idle: at M = 256 (one
+// row of 32 wide tiles on 76 pairs) 21-22 us against 24-25 us.
+constexpr double kNarrowColumnCost = 1.4;
+
+int tile_bn_for(int64_t M, int64_t N, int num_sms, int pinned) {
+  if (pinned) return pinned;
+  const int64_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  const int64_t mp = (M + 2 * kBM - 1) / (2 * kBM);
+  const int64_t tiles_w = mp * ((N + kMxBN - 1) / kMxBN);
+  const int64_t tiles_n = mp * ((N + kMxBNarrow - 1) / kMxBNarrow);
+  const double est_w = static_cast<double>((tiles_w + pairs - 1) / pairs) * kMxBN;
+  const double est_n = static_cast<double>((tiles_n + pairs - 1) / pairs) * kMxBNarrow * kNarrowColumnCost;
+  return est_n < est_w ? kMxBNarrow : kMxBN;
+}
+
+template <int BN>
+sg_status_t launch_pair(const LaunchArgs& a, const RecGeom& g, const uint32_t* rec_a, const uint32_t* rec_b) {
+  using T = MxTile<BN>;
+  CUtensorMap tmA, tmB, tmRA, tmRB, tmC;
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, 128, kBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, T::kBHalf,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmRA, CU_TENSOR_MAP_DATA_TYPE_UINT32, rec_a, kRec / 4, g.a_records(), kRec, kRec / 4, 1,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tmRB, CU_TENSOR_MAP_DATA_TYPE_UINT32, rec_b, kRec / 4, g.b_rows(), kRec, kRec / 4,
+                 T::kSfBRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols, kCBoxRows,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
+    return SG_ERR_CUDA;
+  GemmParams p{};
+  p.M = static_cast<int32_t>(a.M);
+  p.N = static_cast<int32_t>(a.N);
+  p.K = static_cast<int32_t>(a.K);
+  p.m_blocks = static_cast<int32_t>((a.M + kBM - 1) / kBM);
+  p.n_blocks = static_cast<int32_t>((a.N + BN - 1) / BN);
+  p.k_blocks = static_cast<int32_t>((a.K + 127) / 128);
+  p.num_tiles = p.m_blocks * p.n_blocks;
+  p.skip_kstep = a.skip_kstep;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
+  const int max_pairs = a.num_sms / 2;
+  const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pairs * 2, 1, 1);
+  cfg.blockDim = dim3(kMxThreads, 1, 1);
+  cfg.dynamicSmemBytes = MxLayout<BN>::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mxfp8_pair_kernel<BN>, tmA, tmB, tmRA, tmRB, tmC, p);
+  if (e != cudaSuccess) {
+    note_cuda_error(e);
+    cudaGetLastError();  // clear the non-sticky launch error
+    return SG_ERR_CUDA;
+  }
+  return SG_OK;
 }
 
 }  // namespace
 
+// Both widths' records fit: the wide tiles' B records (8 rows per 224 columns)
+// outnumber the narrow tiles' (1 row per 128 columns) for every N.
 size_t mxfp8_workspace_bytes(int64_t M_max, int64_t N, int64_t K) {
-  const RecGeom g = rec_geom(M_max, N, K);
+  const RecGeom g = rec_geom(M_max, N, K, kMxBN);
   return static_cast<size_t>(g.a_records() + g.b_rows()) * kRec;
 }
 
 cudaError_t mxfp8_prepare() {
-  return cudaFuncSetAttribute(mxfp8_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              MxLayout::kDynSmem);
+  const cudaError_t e = cudaFuncSetAttribute(mxfp8_pair_kernel<kMxBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             MxLayout<kMxBN>::kDynSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mxfp8_pair_kernel<kMxBNarrow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              MxLayout<kMxBNarrow>::kDynSmem);
 }
 
+bool mxfp8_tile_ok(int bn) { return bn == kMxBN || bn == kMxBNarrow; }
+
 sg_status_t mxfp8_launch(const LaunchArgs& a) {
-  const RecGeom g = rec_geom(a.M, a.N, a.K);
-  // B's records first: their count depends on N and K only, so A's (which grow
-  // with M) start at the same place for every M <= M_max.
+  const int bn = tile_bn_for(a.M, a.N, a.num_sms, a.tile_bn);
+  const RecGeom g = rec_geom(a.M, a.N, a.K, bn);
+  // B's records first: their count depends on N, K and the width only, so A's
+  // (which grow with M) never overlap them.
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   uint32_t* rec_b = reinterpret_cast<uint32_t*>(ws);
   uint32_t* rec_a = reinterpret_cast<uint32_t*>(ws + g.b_rows() * kRec);
@@ -425,58 +555,15 @@ sg_status_t mxfp8_launch(const LaunchArgs& a) {
     const sg_status_t st = launch_status();
     if (st != SG_OK) return st;
   }
-  CUtensorMap tmA, tmB, tmRA, tmRB, tmC;
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.A, a.K, a.M, a.K, 128, kBM,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kMxBHalf,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmRA, CU_TENSOR_MAP_DATA_TYPE_UINT32, rec_a, kRec / 4, g.a_records(), kRec, kRec / 4, 1,
-                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_2d(&tmRB, CU_TENSOR_MAP_DATA_TYPE_UINT32, rec_b, kRec / 4, g.b_rows(), kRec, kRec / 4, 8,
-                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols, kCBoxRows,
-                 CU_TENSOR_MAP_SWIZZLE_64B))
-    return SG_ERR_CUDA;
-  GemmParams p{};
-  p.M = static_cast<int32_t>(a.M);
-  p.N = static_cast<int32_t>(a.N);
-  p.K = static_cast<int32_t>(a.K);
-  p.m_blocks = static_cast<int32_t>((a.M + kBM - 1) / kBM);
-  p.n_blocks = static_cast<int32_t>((a.N + kMxBN - 1) / kMxBN);
-  p.k_blocks = static_cast<int32_t>((a.K + 127) / 128);
-  p.num_tiles = p.m_blocks * p.n_blocks;
-  p.skip_kstep = a.skip_kstep;
-  p.status = a.status;
-  p.timeout_ns = a.timeout_ns;
-  const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
-  const int max_pairs = a.num_sms / 2;
-  const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pairs * 2, 1, 1);
-  cfg.blockDim = dim3(kMxThreads, 1, 1);
-  cfg.dynamicSmemBytes = MxLayout::kDynSmem;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, mxfp8_pair_kernel, tmA, tmB, tmRA, tmRB, tmC, p);
-  if (e != cudaSuccess) {
-    note_cuda_error(e);
-    cudaGetLastError();  // clear the non-sticky launch error
-    return SG_ERR_CUDA;
-  }
-  return SG_OK;
+  return bn == kMxBN ? launch_pair<kMxBN>(a, g, rec_a, rec_b) : launch_pair<kMxBNarrow>(a, g, rec_a, rec_b);
 }
 
-void mxfp8_config(TileConfig* c) {
+void mxfp8_config(int64_t M, int64_t N, int num_sms, int tile_bn, TileConfig* c) {
+  const int bn = tile_bn_for(M, N, num_sms, tile_bn);
   c->bm = kBM;
-  c->bn = kMxBN;
+  c->bn = bn;
   c->bk = 128;
-  c->stages = kMxStages;
+  c->stages = bn == kMxBN ? MxTile<kMxBN>::kStages : MxTile<kMxBNarrow>::kStages;
   c->cluster = 2;
   c->rows_per_group = 2 * kBM;
 }

@@ -125,11 +125,24 @@ sg_status_t scaled_gemm_destroy(sg_handle_t h);
 /* A static English description of a status code. */
 const char* scaled_gemm_status_string(sg_status_t s);
 
-/* Tile geometry the plan launches with: BM x BN output tiles per CTA, BK elements
- * of K per pipeline stage, `stages` shared-memory stages, `grid` persistent CTAs for
- * M = M_max (whole clusters, where the kernel runs CTAs in pairs).  Any output
+/* Tile geometry of a launch at M = M_max: BM x BN output tiles per CTA (BN: the
+ * tile's columns; CTA pairs share a BN-wide tile), BK elements of K per pipeline
+ * stage, `stages` shared-memory stages, `grid` persistent CTAs (whole clusters,
+ * where the kernel runs CTAs in pairs).  mxfp8 chooses BN per launch from M and N
+ * (see scaled_gemm_set_tile), so a smaller M may use the other width.  Any output
  * pointer may be NULL.                                                           */
 sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int* stages, int* grid);
+
+/* Pin the output-tile width every later launch of the plan uses, or pass 0 to let
+ * each launch choose (the default).  mxfp8 has two widths: 224 (256 x 224 tiles per
+ * CTA pair) and 128 (256 x 128); a launch chooses 128 where 224-wide tiles would
+ * leave pairs of SMs idle (small M), by an estimate of waves of tiles x width.
+ * The other modes have one width (256) and accept only 0 or that width.  Both
+ * widths sum every output element over K in the same order of MMA instructions.
+ * Not to be called while a launch of the plan is being enqueued from another
+ * thread.
+ * Returns SG_ERR_INVALID_ARG for a NULL handle or a width the mode does not have. */
+sg_status_t scaled_gemm_set_tile(sg_handle_t h, int bn);
 
 /* Read and clear the plan's device status word: synchronises `stream`, then stores
  * SG_OK or SG_ERR_TIMEOUT in *code and, for a timeout, the role / wait site that gave

@@ -73,6 +73,7 @@ def test_null_handle_is_rejected(lib):
     assert L.scaled_gemm_destroy(None) == 0
     assert L.scaled_gemm_get_config(None, None, None, None, None, None) == 1
     assert L.scaled_gemm_set_debug(None, 0, -1) == 1
+    assert L.scaled_gemm_set_tile(None, 0) == 1
     code = ctypes.c_int32()
     assert L.scaled_gemm_debug_status(None, None, ctypes.byref(code), None) == 1
     assert L.scaled_gemm_create(None, 1, 256, 256, 16, -1) == 1

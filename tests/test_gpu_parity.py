@@ -30,12 +30,15 @@ def gpu():
     return gpu_util
 
 
-def _run_full(gpu, case, launches=20):
-    """Full comparison against the oracle on every launch."""
+def _run_full(gpu, case, launches=20, tile_bn=0):
+    """Full comparison against the oracle on every launch (`tile_bn`: the plan's
+    pinned output-tile width, 0 = chosen per launch)."""
     _, ref = oracle.gemm(case.mode, *case.numpy(), want_r=False)
     dc = gpu.DeviceCase(case)
     h = gpu.make_plan(case)
     try:
+        if tile_bn:
+            gpu.binding.scaled_gemm_set_tile(h, tile_bn)
         first = None
         for i in range(launches):
             dc.poison()
@@ -145,6 +148,43 @@ def test_mxfp8_shapes(gpu, M, N, K):
 )
 def test_blockscale_shapes(gpu, M, N, K):
     _run_full(gpu, synth.make_case("blockscale", M, N, K, seed=M + K, b_std=0.02), launches=8)
+
+
+@pytest.mark.parametrize(
+    "M,N,K",
+    [
+        (1, 16, 32),         # one row, 16 of a tile's 128 columns, one K block of 32
+        (200, 448, 1024),    # ragged M, 3.5 tiles of 128 columns
+        (383, 672, 2080),    # odd number of 128-row chunks, partial last tile, ragged last K step
+        (256, 7168, 1792),   # the workload's N and K at one pair row (the automatic choice is narrow)
+        (2304, 1280, 384),   # 90 pair tiles on 76 pairs: second tiles, both accumulators
+    ],
+)
+def test_mxfp8_narrow_tiles(gpu, M, N, K):
+    # 256 x 128 pair tiles: B staged 64 rows per CTA, B's scales in 512-byte records
+    _run_full(gpu, synth.make_case("mxfp8", M, N, K, seed=M + K + 1, b_std=0.02), launches=8, tile_bn=128)
+
+
+def test_mxfp8_tile_width_follows_m(gpu):
+    # a plan reports the width of a launch at M_max: 128 where 224-wide tiles would
+    # leave pairs of SMs idle, 224 otherwise; set_tile pins a width or restores the choice
+    b = gpu.binding
+    small = b.scaled_gemm_create("mxfp8", 7168, 1792, 256)
+    large = b.scaled_gemm_create("mxfp8", 7168, 1792, 32768)
+    dense = b.scaled_gemm_create("ptpc", 7168, 1792, 256)
+    try:
+        assert b.scaled_gemm_get_config(small)["bn"] == 128
+        assert b.scaled_gemm_get_config(large)["bn"] == 224
+        b.scaled_gemm_set_tile(large, 128)
+        assert b.scaled_gemm_get_config(large)["bn"] == 128
+        b.scaled_gemm_set_tile(large, 0)
+        assert b.scaled_gemm_get_config(large)["bn"] == 224
+        L = b.lib()
+        assert L.scaled_gemm_set_tile(large, 256) == 1 and L.scaled_gemm_set_tile(large, 96) == 1
+        assert L.scaled_gemm_set_tile(dense, 128) == 1 and L.scaled_gemm_set_tile(dense, 256) == 0
+    finally:
+        for h in (small, large, dense):
+            b.scaled_gemm_destroy(h)
 
 
 def test_mxfp8_back_to_back_launches_on_one_plan(gpu):
