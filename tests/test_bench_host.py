@@ -1,5 +1,7 @@
 """Host-side logic of bench.py without a GPU: the replica control plane (gloo,
-two ranks on the CPU) and the whole-job throughput aggregation."""
+two ranks on the CPU), the whole-job throughput aggregation, and the rule that a
+stored DRAM-traffic figure is reported only for the kernel sources it was
+measured on."""
 import os
 import socket
 
@@ -64,3 +66,40 @@ def test_suite_covers_every_mode_and_the_unpadded_shapes():
     assert {6288, 3648, 6400, 7168, 896} <= ns
     assert synth.gemm_flops(32768, 6400, 7168) == pytest.approx(3006.5e9, rel=1e-4)
     assert synth.gemm_bytes("ptpc", 32768, 6400, 7168) == pytest.approx(700.3e6, rel=1e-3)
+
+
+def _traffic_rows():
+    import bench
+
+    rows = []
+    for line in open(os.path.join(bench.ROOT, "profiles", "traffic.txt")):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#"):
+            rows.append((f[0], f[1], float(f[2])))
+    return rows
+
+
+def test_stored_traffic_applies_only_to_the_sources_it_was_measured_on(monkeypatch):
+    # the roofline's DRAM traffic comes from a capture of one revision of a kernel's
+    # sources; for any other revision it is not reported (null)
+    import bench
+    import synth
+
+    rows = _traffic_rows()
+    assert rows, "profiles/traffic.txt has no rows"
+    for workload, rev, nbytes in rows:
+        assert workload in synth.CONFIGS
+        current = bench.kernel_revision(synth.CONFIGS[workload][0])
+        assert bench.stored_traffic(workload) == (nbytes if rev == current else None)
+    monkeypatch.setattr(bench, "kernel_revision", lambda mode="ptpc": "000000000000")
+    assert all(bench.stored_traffic(w) is None for w, _, _ in rows)
+
+
+def test_kernel_revision_hashes_each_family_s_own_sources():
+    import bench
+
+    revs = {m: bench.kernel_revision(m) for m in ("ptpc", "mxfp8", "blockscale")}
+    assert len(set(revs.values())) == 3
+    assert all(len(r) == 12 for r in revs.values())
+    assert bench.kernel_revision("bf16") == revs["ptpc"]  # one kernel file for both
+    assert revs == {m: bench.kernel_revision(m) for m in revs}
