@@ -185,6 +185,17 @@ def test_mxfp8_tile_width_follows_m(gpu):
     finally:
         for h in (small, large, dense):
             b.scaled_gemm_destroy(h)
+    from fp8_scaled_gemm_sm_gb300 import ScaledGemm
+
+    op = ScaledGemm("mxfp8", 7168, 1792, 32768)
+    try:
+        assert op.config()["bn"] == 224
+        op.set_tile(128)
+        assert op.config()["bn"] == 128
+        op.set_tile()
+        assert op.config()["bn"] == 224
+    finally:
+        op.close()
 
 
 def test_mxfp8_back_to_back_launches_on_one_plan(gpu):
