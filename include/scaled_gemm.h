@@ -135,8 +135,10 @@ sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int
 
 /* Pin the output-tile width every later launch of the plan uses, or pass 0 to let
  * each launch choose (the default).  mxfp8 has two widths: 224 (256 x 224 tiles per
- * CTA pair) and 128 (256 x 128); a launch chooses 128 where 224-wide tiles would
- * leave pairs of SMs idle (small M), by an estimate of waves of tiles x width.
+ * CTA pair) and 128 (256 x 128, the narrow mxfp8 tile ROCm/mori PR 785 names in its
+ * Test section); a launch chooses 128 where 224-wide tiles would leave pairs of SMs
+ * idle (small M), by an estimate of waves of tiles x width (the shape-aware default
+ * a review of ROCm/mori PR 809, Smaller points, asks for).
  * The other modes have one width (256) and accept only 0 or that width.  Both
  * widths sum every output element over K in the same order of MMA instructions.
  * Not to be called while a launch of the plan is being enqueued from another
