@@ -197,6 +197,106 @@ def cpu_baseline(cases, rows, seconds_cap=None):
     return flops / dt / 1e12, dt, oracle.num_threads(), flops
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+C0_ONE_CORE = r"""
+import json, sys, time
+sys.path.insert(0, %r)
+import oracle, synth
+mode, M, N, K, seed, a, b = synth.CONFIGS["c0_ptpc_256x512x256"]
+c = synth.make_case(mode, M, N, K, seed=seed, a_std=a, b_std=b)
+args = c.numpy()
+oracle.gemm(mode, *args, want_r=False)
+t0 = time.perf_counter()
+oracle.gemm(mode, *args, want_r=False)
+dt = time.perf_counter() - t0
+print(json.dumps({"seconds": dt, "gflops": c.flops / dt / 1e9, "threads": oracle.num_threads()}))
+"""
+
+
+def c0_one_core():
+    """The oracle on the whole 256 x 512 x 256 ptpc workload with one OpenMP thread
+    (a child process started with OMP_NUM_THREADS=1)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", C0_ONE_CORE % ROOT], capture_output=True, text=True, env=env,
+                           timeout=300)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"workload": "c0_ptpc_256x512x256", "seconds": round(d["seconds"], 4),
+                "gflops": round(d["gflops"], 3), "threads": d["threads"]}
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError, KeyError) as e:
+        return {"workload": "c0_ptpc_256x512x256", "error": str(e)[:200]}
+
+
+def choose_peak(clk):
+    """Burst or sustained FP8 / BF16 peak for this run, from its clock record: the
+    burst figure (a short cuBLAS burst at full clock) when the SM clock held within
+    3% of its maximum with no power cap active during the timed region, else the
+    sustained one (a seconds-long loop under the power cap).  Returns (kind, why)."""
+    sm, smax, reasons = clk.get("sm_mhz"), clk.get("sm_max_mhz"), clk.get("reasons") or []
+    if sm is None or not smax:
+        return "sustained", "no clock record"
+    if "sw_power_cap" in reasons:
+        return "sustained", "sw_power_cap was active (median SM clock %.0f of %.0f MHz)" % (sm, smax)
+    if sm < 0.97 * smax:
+        return "sustained", "median SM clock %.0f MHz < 0.97 x max %.0f" % (sm, smax)
+    return "burst", "median SM clock %.0f of %.0f MHz, no power cap" % (sm, smax)
+
+
+# Workloads shorter than this are also timed per call in a CUDA graph.
+GRAPH_MAX_US = 100.0
+
+
+def graph_per_call(launch_fn, stream, calls=200, batches=9):
+    """Median device time per call over `batches` replays of a CUDA graph of
+    `calls` back-to-back launches on the same operands (deepseek-ai/DeepGEMM PR
+    453, Performance Overhead: CUDA-graph median per call over 9 x 200 calls).
+    The operands stay in L2 between calls where they fit."""
+    try:
+        with torch.cuda.stream(stream):
+            launch_fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(calls):
+                launch_fn()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(batches):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            per.append(1e3 * e0.elapsed_time(e1) / calls)
+        del g
+        return {"us_median": round(statistics.median(per), 2), "us_min": round(min(per), 2),
+                "calls": calls, "batches": batches}
+    except RuntimeError as e:
+        return {"error": str(e)[:200]}
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 
@@ -207,9 +307,8 @@ def run_gpu(args, control, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_kind = load_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    fp8_peak_sustained = 2.0 * peaks["bf16_tflops_sustained"]
     fp8_peak_burst = 2.0 * peaks["bf16_tflops"]
-    bf16_peak = peaks["bf16_tflops_sustained"]
     hbm = peaks["hbm_gbs"]
 
     cases = make_suite(args.only, args.rows)
@@ -268,6 +367,9 @@ def run_gpu(args, control, rank, local):
     wall1 = time.perf_counter()
     clk = clocks.stop()
     local_s = e_all0.elapsed_time(e_all1) / 1e3
+    peak_kind_run, peak_why = choose_peak(clk)
+    fp8_peak = fp8_peak_burst if peak_kind_run == "burst" else fp8_peak_sustained
+    bf16_peak = peaks["bf16_tflops"] if peak_kind_run == "burst" else peaks["bf16_tflops_sustained"]
     flops_step = sum(d["case"].flops for d in work)
     total_flops, t_max, value = aggregate(control, flops_step * args.steps, local_s)
 
@@ -285,6 +387,7 @@ def run_gpu(args, control, rank, local):
             "tflops": round(tf, 1),
             "frac_peak": round(tf / peak, 3),
             "frac_peak_burst": round(tf / (peaks["bf16_tflops"] if c.mode == "bf16" else fp8_peak_burst), 3),
+            "frac_peak_sustained": round(tf / (peaks["bf16_tflops_sustained"] if c.mode == "bf16" else fp8_peak_sustained), 3),
             "gbs": round(byts / (us * 1e-6) / 1e9, 1),
             "frac_hbm": round(byts / (us * 1e-6) / 1e9 / hbm, 3),
             "tile": "%dx%d" % (d["cfg"]["bm"], d["cfg"]["bn"]), "grid": d["cfg"]["grid"],
@@ -301,13 +404,22 @@ def run_gpu(args, control, rank, local):
     dom_flops = 2.0 * pc["M"] * pc["N"] * pc["K"]
     achieved = dom_flops / (pc["us"] * 1e-6) / 1e12
     dom_peak = bf16_peak if pc["mode"] == "bf16" else fp8_peak
+    # the same kernel over all of its launches in the step (every workload it runs)
+    dom_all = [k for k in per if per[k]["mode"] == dom_mode]
+    all_flops = sum(2.0 * per[k]["M"] * per[k]["N"] * per[k]["K"] for k in dom_all)
+    all_us = sum(per[k]["us"] for k in dom_all)
+    achieved_all = all_flops / (all_us * 1e-6) / 1e12
     traffic = stored_traffic(dom)
     roofline = {
         "bound": "tensor", "achieved": round(achieved, 1), "peak": round(dom_peak, 1), "unit": "TFLOP/s",
         "frac": round(achieved / dom_peak, 3), "traffic": traffic,
         "kernel": kernel_name(pc["mode"], pc["K"]),
         "workload": dom,
-        "peak_source": "%s: 2 x bf16_tflops_sustained (fp8 = 2 x bf16 nominal ratio)" % peak_kind,
+        "achieved_all_launches": round(achieved_all, 1),
+        "frac_all_launches": round(achieved_all / dom_peak, 3),
+        "launches_per_step": len(dom_all),
+        "peak_source": "%s: 2 x bf16_tflops%s (fp8 = 2 x bf16 nominal ratio); %s peak because %s" % (
+            peak_kind, "" if peak_kind_run == "burst" else "_sustained", peak_kind_run, peak_why),
     }
 
     # bad launches: 20 launches per workload into NaN-poisoned outputs, each
@@ -334,8 +446,13 @@ def run_gpu(args, control, rank, local):
         code, _ = binding.scaled_gemm_debug_status(d["h"], sraw)
         status_bad += code != 0
 
+    if not args.no_graph:
+        for d in work:
+            if per[d["name"]]["us"] < GRAPH_MAX_US:
+                per[d["name"]]["graph"] = graph_per_call(lambda d=d: launch(d), stream)
+
     quant = None if args.no_quant else run_quantize(binding, dev, stream, hbm)
-    extra = None if (args.no_quant or args.only) else run_extra(binding, dev, stream, local, fp8_peak)
+    extra = None if (args.no_quant or args.only) else run_extra(binding, dev, stream, local, fp8_peak_burst)
 
     # end to end through the C ABI with host buffers: H2D inputs, GEMM, D2H C
     e2e = None if args.no_e2e else run_e2e(work, launch, stream, args, control, dev)
@@ -344,8 +461,9 @@ def run_gpu(args, control, rank, local):
     if rank == 0 and control.world == 1 and not args.no_cpu_baseline:
         v, dt, cores, fl = cpu_baseline(cases, args.cpu_rows)
         cpu = {
-            "value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": "rows [0,%d) of every suite workload (%.1f GFLOP, %.1f s)" % (args.cpu_rows, fl / 1e9, dt),
+            "c0_one_core": c0_one_core(),
         }
 
     for d in work:
@@ -374,8 +492,9 @@ def run_gpu(args, control, rank, local):
                          "watchdog_timeouts": status_bad},
         "per_config": per,
         "wall_s_timed": round(wall1 - wall0, 4),
-        "peaks": {"source": peak_kind, "fp8_tflops_sustained": fp8_peak, "fp8_tflops_burst": fp8_peak_burst,
-                  "bf16_tflops_sustained": bf16_peak, "hbm_gbs": hbm},
+        "peaks": {"source": peak_kind, "used": peak_kind_run, "fp8_tflops_sustained": fp8_peak_sustained,
+                  "fp8_tflops_burst": fp8_peak_burst, "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+                  "bf16_tflops_burst": peaks["bf16_tflops"], "hbm_gbs": hbm},
     }
     return line
 
@@ -390,11 +509,10 @@ def kernel_name(mode, K):
         return "mxfp8_pair_kernel"
     if mode == "blockscale":
         return "blockscale_pair_kernel"
-    short = (K + (63 if mode == "bf16" else 127)) // (64 if mode == "bf16" else 128) <= 4
-    return ("dense_gemm_kernel<%s, short K>" if short else "dense_pair_kernel<%s>") % mode
+    return "dense_pair_kernel<%s>" % mode
 
 
-def run_extra(binding, dev, stream, local, fp8_peak, iters=20):
+def run_extra(binding, dev, stream, local, fp8_peak_burst, iters=20):
     """Shapes outside the suite (not part of `value`), each timed on its own:
     3 warm-up launches, then `iters` launches between CUDA events; inputs plus
     output are larger than L2.  Includes the gather-GEMM workload (16384 rows
@@ -423,7 +541,7 @@ def run_extra(binding, dev, stream, local, fp8_peak, iters=20):
         us = 1e3 * e0.elapsed_time(e1) / iters
         tf = c.flops / (us * 1e-6) / 1e12
         out[name] = {"mode": mode, "M": M, "N": N, "K": K, "us": round(us, 2), "tflops": round(tf, 1),
-                     "frac_peak": round(tf / fp8_peak, 3), "kernel": kernel_name(mode, K)}
+                     "frac_peak_burst": round(tf / fp8_peak_burst, 3), "kernel": kernel_name(mode, K)}
         binding.scaled_gemm_destroy(h)
         del A, B, sa, sb, C
     for name, (M, R, N, K, seed) in synth.GATHER_CONFIGS.items():
@@ -447,8 +565,8 @@ def run_extra(binding, dev, stream, local, fp8_peak, iters=20):
         tf = c.flops / (us * 1e-6) / 1e12
         byts = M * K + N * K + 2.0 * M * N + 4.0 * (2 * M + N)  # gathered A, B, C, a/b scales, idx
         out[name] = {"mode": "ptpc gather", "M": M, "N": N, "K": K, "R": R, "us": round(us, 2),
-                     "tflops": round(tf, 1), "frac_peak": round(tf / fp8_peak, 3),
-                     "gbs": round(byts / (us * 1e-6) / 1e9, 1), "kernel": "dense_gemm_kernel<ptpc, gather>"}
+                     "tflops": round(tf, 1), "frac_peak_burst": round(tf / fp8_peak_burst, 3),
+                     "gbs": round(byts / (us * 1e-6) / 1e9, 1), "kernel": "gather_gemm_kernel"}
         binding.scaled_gemm_destroy(h)
         del A, sa, idx, B, sb, C
     return out
@@ -662,6 +780,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--no-quant", action="store_true", help="skip the quantisation measurement (profiling runs)")
     ap.add_argument("--no-bad-check", action="store_true", help="skip the 20-launch check (profiling runs)")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph per-call timing (profiling runs)")
     ap.add_argument("--only", default=None, choices=synth.SUITE + synth.EXTRA, help="one workload (profiling runs)")
     ap.add_argument("--rows", type=int, default=None, help="override M of the workload(s) (profiling runs)")
     args = ap.parse_args(argv)

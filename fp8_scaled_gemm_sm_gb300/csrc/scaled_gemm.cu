@@ -283,15 +283,15 @@ sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, cons
   if (!scaled && (a_scale || b_scale)) return fail(SG_ERR_INVALID_ARG, "launch: bf16 takes no scales");
   if (!aligned16(A) || !aligned16(B)) return fail(SG_ERR_MISALIGNED, "launch: A or B");
   if (scaled && (!aligned16(a_scale) || !aligned16(b_scale))) return fail(SG_ERR_MISALIGNED, "launch: scales");
-  // C must not overlap an operand (the kernel streams C while it still reads them).
+  // C must not overlap an operand or a scale buffer (the kernel streams C out
+  // while it still reads them).
   const int64_t el = h->mode == SG_MODE_BF16 ? 2 : 1;
-  auto overlap = [](const void* p, int64_t pb, const void* q, int64_t qb) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
-    return a < b + static_cast<uintptr_t>(qb) && b < a + static_cast<uintptr_t>(pb);
-  };
   const int64_t cb = M * h->N * 2;
-  if (overlap(C, cb, A, M * h->K * el) || overlap(C, cb, B, h->N * h->K * el))
+  if (sg::ranges_overlap(C, cb, A, M * h->K * el) || sg::ranges_overlap(C, cb, B, h->N * h->K * el))
     return fail(SG_ERR_INVALID_ARG, "launch: C overlaps A or B");
+  if (sg::ranges_overlap(C, cb, a_scale, sg::scale_bytes_a(h->mode, M, h->K)) ||
+      sg::ranges_overlap(C, cb, b_scale, sg::scale_bytes_b(h->mode, h->N, h->K)))
+    return fail(SG_ERR_INVALID_ARG, "launch: C overlaps a scale buffer");
 
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return fail(SG_ERR_CUDA, "launch: cudaGetDevice");
@@ -345,13 +345,11 @@ sg_status_t scaled_gemm_launch_gather(sg_handle_t h, const void* A_src, int64_t 
     return fail(SG_ERR_INVALID_ARG, "launch_gather: NULL operand");
   if (!aligned16(A_src) || !aligned16(idx) || !aligned16(B) || !aligned16(a_scale_src) || !aligned16(b_scale))
     return fail(SG_ERR_MISALIGNED, "launch_gather: operand");
-  auto overlap = [](const void* p, int64_t pb, const void* q, int64_t qb) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
-    return a < b + static_cast<uintptr_t>(qb) && b < a + static_cast<uintptr_t>(pb);
-  };
   const int64_t cb = M * h->N * 2;
-  if (overlap(C, cb, A_src, R * h->K) || overlap(C, cb, B, h->N * h->K) || overlap(C, cb, idx, M * 4))
-    return fail(SG_ERR_INVALID_ARG, "launch_gather: C overlaps an operand");
+  if (sg::ranges_overlap(C, cb, A_src, R * h->K) || sg::ranges_overlap(C, cb, B, h->N * h->K) ||
+      sg::ranges_overlap(C, cb, idx, M * 4) || sg::ranges_overlap(C, cb, a_scale_src, 4 * R) ||
+      sg::ranges_overlap(C, cb, b_scale, 4 * h->N))
+    return fail(SG_ERR_INVALID_ARG, "launch_gather: C overlaps an operand or a scale buffer");
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return fail(SG_ERR_CUDA, "launch_gather: cudaGetDevice");
   if (cur != h->device) return fail(SG_ERR_INVALID_ARG, "launch_gather: current device differs from the plan's");

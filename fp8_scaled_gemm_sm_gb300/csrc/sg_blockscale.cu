@@ -98,7 +98,6 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   constexpr uint32_t kIdesc = instr_desc(0, 0, 2 * kBM, kBsBN);
   constexpr uint32_t kTxPair = 2 * (L::kAStage + L::kBStage);  // both CTAs' bytes
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint16_t kBoth = 0x3;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -220,8 +219,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k)
             mma_f8f6f4_pair(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k), kIdesc, k != 0);
-          mma_commit_pair(empty_bar(stage), kBoth);
-          mma_commit_pair(pfull_bar(part), kBoth);
+          mma_commit_pair_both(empty_bar(stage));
+          mma_commit_pair_both(pfull_bar(part));
           if (++stage == kBpStages) {
             stage = 0;
             phase ^= 1;
@@ -233,7 +232,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
       }
       if (!ok) {
-        mma_commit_pair(drain_bar, 0x1);
+        mma_commit_pair(drain_bar);
         mbar_wait_drain(drain_bar, 0, 200000000ull);
       }
     }

@@ -3,19 +3,25 @@
 //   C[m,n] = bf16(acc[m,n] * a_scale[m] * b_scale[n])   (ptpc, e4m3 x e4m3)
 //   C[m,n] = bf16(acc[m,n])                             (bf16 x bf16)
 //
-// Per CTA (one per SM, persistent over output tiles of 128 x BN):
-//   warp 0      TMA producer: waits empty[s], arms full[s] with the stage's byte
-//               count and loads the A tile [128 x 128 B] and B tile [BN x 128 B]
-//               (128-byte swizzle) into stage s of the shared-memory ring.
-//   warp 1      allocates TMEM (two BN-column fp32 accumulators); one thread
-//               waits full[s], issues 4 tcgen05.mma (K = 32 fp8 / 16 bf16 each)
-//               and commits to empty[s], so a stage is handed back only after
-//               the tensor core has finished reading it; after a tile's last K
-//               block it commits to tmem_full[acc].
-//   warps 2..   epilogue: wait tmem_full[acc], read the accumulator with
-//               tcgen05.ld, scale, round to bf16, stage in shared memory, fence
-//               the async proxy, store by TMA; release the accumulator with
-//               tcgen05.fence::before_thread_sync + arrive on tmem_empty[acc].
+// Every K runs on CTA pairs (a cluster of two CTAs on neighbouring SMs), each
+// pair persistent over 256 x BN output tiles computed with the pair MMA
+// (tcgen05.mma.cta_group::2).  Per CTA:
+//   warp 0      TMA producer: waits empty[s], loads this CTA's A rows [128 x
+//               128 B] and its half of the tile's B rows [BN/2 x 128 B] (128-byte
+//               swizzle) into stage s; the bytes of both CTAs complete the even
+//               CTA's full[s], which its producer arms.
+//   warp 1      allocates TMEM with the peer (two BN-column fp32 accumulators);
+//               in the even CTA one thread waits full[s], issues 4 pair MMAs
+//               (K = 32 fp8 / 16 bf16 each) and commits to empty[s] of both
+//               CTAs, so a stage is handed back only after the tensor cores have
+//               finished reading it; after a tile's last K block it commits to
+//               tmem_full[acc] of both CTAs.
+//   warps 2..   epilogue: wait tmem_full[acc], read this CTA's 128 accumulator
+//               rows with tcgen05.ld, scale, round to bf16, stage in shared
+//               memory, fence the async proxy, store by TMA; hand the
+//               accumulator back with tcgen05.fence::before_thread_sync + an
+//               arrive on the even CTA's tmem_empty[acc].
+// A gather variant (ptpc, one CTA per SM, A rows gathered by index) follows.
 //
 // The stage / phase counters run continuously across tiles, so a K loop of one
 // or two blocks (the "peeled tail" case, K <= 256) goes through exactly the
@@ -26,7 +32,8 @@
 // (deepseek-ai/DeepGEMM PR 453, ds-review-bot v4: "release smem only after
 // UMMA commits").  The epilogue's generic shared-memory writes are fenced into
 // the async proxy by every writing thread before the TMA store is issued
-// (deepseek-ai/DeepGEMM PR 453, Fix).
+// (deepseek-ai/DeepGEMM PR 453, Fix).  No TMA load here is multicast: every
+// CTA loads its own operand rows from this GPU's memory.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,314 +41,6 @@
 #include "sg_internal.h"
 
 namespace sg {
-
-template <int BN, int STAGES, int EPI_WARPS, int NBOX, int BOXW>
-struct DenseLayout {
-  static constexpr int kAStage = kBM * kRowBytes;
-  static constexpr int kBStage = BN * kRowBytes;
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + STAGES * kAStage;
-  static constexpr int kOffC = kOffB + STAGES * kBStage;
-  static constexpr int kOffScale = kOffC + EPI_WARPS * NBOX * cbox_bytes<BOXW>();  // per-warp column scales
-  static constexpr int kScaleCols = BN * 4 / EPI_WARPS;                   // columns per warp
-  static constexpr int kOffBar = kOffScale + EPI_WARPS * kScaleCols * 4;
-  static constexpr int kNumBars = 2 * STAGES + 5;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16 + 4 * STAGES;
-  static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
-  static_assert(kOffC % 1024 == 0, "store boxes need 512-byte alignment");
-};
-
-// GATHER (ptpc only): output row m reads source row p.gather_idx[m] of the source
-// A [rows_src][K] and its scale a_scale[gather_idx[m]] (ROCm/aiter PR 6539,
-// Technical Details: the gather_kv_b_proj kernel gathers its A rows inside the
-// GEMM's pipeline).  Two more warps (after the epilogue warps) copy the tile's
-// rows into the stage with 16-byte cp.async, eight lanes per row, writing the
-// 128-byte-swizzled layout the MMA reads, and arrive on full[s] as their copies
-// complete; B still comes by TMA.  (Gathering with TMA tile::gather4 took 33
-// copy operations per stage instead of 2 and ran 2.5x slower than the plain
-// GEMM, bound by the TMA unit.)  An index outside [0, rows_src) -- and every row
-// past M -- reads source row 0 and gets scale 0, so no copy leaves the source
-// and such a row's output is zero (or clipped).
-template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW, bool GATHER = false>
-__global__ void __launch_bounds__(64 + 32 * EPI_WARPS + (GATHER ? 64 : 0), 1)
-    dense_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using L = DenseLayout<BN, STAGES, EPI_WARPS, NBOX, BOXW>;
-  constexpr bool kScaled = (MODE == kModePtpc);
-  constexpr int kBK = (MODE == kModeBf16) ? 64 : 128;       // K elements per stage
-  constexpr int kUmmaK = (MODE == kModeBf16) ? 16 : 32;      // K per tcgen05.mma
-  constexpr int kKSteps = kBK / kUmmaK;
-  constexpr uint32_t kIdesc =
-      (MODE == kModeBf16) ? instr_desc(1, 1, kBM, BN) : instr_desc(0, 0, kBM, BN);
-  constexpr uint32_t kTx = GATHER ? L::kBStage : L::kAStage + L::kBStage;  // TMA bytes per stage
-  constexpr int kGatherThreads = GATHER ? 64 : 0;
-  constexpr uint32_t kTmemCols = 512;
-  constexpr int kAccStride = 256;
-  constexpr int kColsPerWarp = BN * 4 / EPI_WARPS;
-  constexpr int kBRowsPerCta = BN / CLUSTER;                 // B rows each CTA loads
-  constexpr uint16_t kClusterMask = (1u << CLUSTER) - 1;
-  static_assert(BN <= 256 && BN % 64 == 0, "BN");
-  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
-  static_assert(CLUSTER == 1 || CLUSTER == 2, "cluster size");
-  static_assert(!GATHER || MODE == kModePtpc, "the gather-GEMM is a ptpc GEMM");
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t sA = smem_addr(smem + L::kOffA);
-  const uint32_t sB = smem_addr(smem + L::kOffB);
-  const uint32_t sC = smem_addr(smem + L::kOffC);
-  const uint32_t bar0 = smem_addr(smem + L::kOffBar);
-  auto full_bar = [&](int s) { return bar0 + 8 * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8 * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
-  uint32_t* last_par = misc + 4;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  // Cluster of CLUSTER CTAs on vertically adjacent tiles (same N block): each CTA
-  // loads BN / CLUSTER rows of the shared B tile and multicasts them to all.
-  const int rank = CLUSTER > 1 ? static_cast<int>(cluster_cta_rank()) : 0;
-  const int group = CLUSTER > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-  const int ngroups = CLUSTER > 1 ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
-  const int num_group_tiles = ((p.m_blocks + CLUSTER - 1) / CLUSTER) * p.n_blocks;
-  auto coord = [&](int tg) {
-    TileCoord c;
-    const int mg = tg / p.n_blocks;
-    c.nb = tg - mg * p.n_blocks;
-    c.mb = mg * CLUSTER + rank;
-    return c;
-  };
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1 + kGatherThreads);  // the producer's arm (+ each gather thread's copies)
-      mbar_init(empty_bar(s), CLUSTER);  // one MMA commit from every CTA that reads the stage's B
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 32 * EPI_WARPS);
-    }
-    mbar_init(drain_bar, 1);
-    misc[1] = 0;
-    fence_mbarrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_addr(&misc[0]), kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  if constexpr (CLUSTER > 1) cluster_sync();  // peers' barriers exist before any multicast
-  tc_fence_after();
-  const uint32_t tmem_base = misc[0];
-  const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
-
-  if (GATHER && warp >= 2 + EPI_WARPS) {
-    // ---------------- A rows gathered by index (64 threads, cp.async) ----------------
-    const int t = (warp - 2 - EPI_WARPS) * 32 + lane;  // 0 .. 63
-    const int c = t & 7;                                // 16-byte chunk of the row's 128-byte K slice
-    const int r0 = t >> 3;                              // rows r0, r0 + 8, ..., r0 + 120 of the tile
-    // row r0 + 8 i, chunk c, at (r0 + 8 i) * 128 + ((c ^ r0) << 4): every row of
-    // this thread has swizzle phase r0
-    const uint32_t dst0 = r0 * kRowBytes + ((c ^ r0) << 4);
-    const uint8_t* A = static_cast<const uint8_t*>(p.a_src);
-    auto load_rows = [&](int tg, int32_t (&rows)[16]) {
-      const int mb = tg < num_group_tiles ? coord(tg).mb : 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int m = mb * kBM + r0 + 8 * i;
-        const int32_t v = (tg < num_group_tiles && m < p.M) ? __ldg(p.gather_idx + m) : 0;
-        rows[i] = (v >= 0 && v < p.rows_src) ? v : 0;
-      }
-    };
-    int32_t next[16];
-    load_rows(group, next);
-    int stage = 0, kstep = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int tg = group; tg < num_group_tiles && ok; tg += ngroups) {
-      int32_t rows[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) rows[i] = next[i];
-      load_rows(tg + ngroups, next);  // one tile ahead
-      for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
-        if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
-          ok = false;
-          break;
-        }
-        if (kstep != p.skip_kstep) {
-          const int kofs = kb * kBK + 16 * c;
-          const uint32_t nbytes = kofs < p.K ? 16u : 0u;  // past K: zeros
-          const int koff = kofs < p.K ? kofs : 0;
-          const uint32_t dst = sA + stage * L::kAStage + dst0;
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            cp_async_16(dst + i * 8 * kRowBytes, A + static_cast<int64_t>(rows[i]) * p.K + koff, nbytes);
-          cp_async_arrive_noinc(full_bar(stage));
-        }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
-    cp_async_wait_all();  // this thread's copies land before the CTA can exit
-  } else if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
-      int stage = 0, kstep = 0;
-      uint32_t phase = 0, issued = 0;
-      bool ok = true;
-      for (int tg = group; tg < num_group_tiles && ok; tg += ngroups) {
-        const TileCoord tc = coord(tg);
-        for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
-            ok = false;
-            break;
-          }
-          if (kstep != p.skip_kstep) {
-            mbar_arrive_expect_tx(full_bar(stage), kTx);
-            if constexpr (!GATHER)  // gathered A rows come from the gather warps
-              tma_load_2d(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, full_bar(stage));
-            if constexpr (CLUSTER > 1)
-              tma_load_2d_multicast(sB + stage * L::kBStage + rank * kBRowsPerCta * kRowBytes, &tmB,
-                                    kb * kBK, tc.nb * BN + rank * kBRowsPerCta, full_bar(stage),
-                                    kClusterMask);
-            else
-              tma_load_2d(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN, full_bar(stage));
-            issued |= 1u << stage;
-            last_par[stage] = phase;
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-      if (!ok) {  // loads still in flight must land before the CTA can exit
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), last_par[s], 200000000ull);
-      } else if (CLUSTER > 1) {
-        // Every peer's MMA commit to this CTA's empty barriers must have landed
-        // before the CTA exits: wait for the release of each stage's last fill.
-        for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      int stage = 0, it = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int tg = group; tg < num_group_tiles && ok; tg += ngroups, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_par = (it >> 1) & 1;
-        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem_base + acc * kAccStride;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, wd, kWhereMmaFull)) {
-            ok = false;
-            break;
-          }
-          if constexpr (GATHER) fence_proxy_async_smem();  // the gather warps' cp.async data, for the MMA
-          tc_fence_after();
-          const uint32_t a0 = sA + stage * L::kAStage;
-          const uint32_t b0 = sB + stage * L::kBStage;
-#pragma unroll
-          for (int k = 0; k < kKSteps; ++k) {
-            const uint64_t ad = kmajor_sw128_desc(a0 + k * kUmmaK * (kRowBytes / kBK));
-            const uint64_t bd = kmajor_sw128_desc(b0 + k * kUmmaK * (kRowBytes / kBK));
-            if constexpr (MODE == kModeBf16)
-              mma_f16(d, ad, bd, kIdesc, (kb | k) != 0);
-            else
-              mma_f8f6f4(d, ad, bd, kIdesc, (kb | k) != 0);
-          }
-          // The stage is free once every CTA that received its B half has read it.
-          if constexpr (CLUSTER > 1)
-            mma_commit_multicast(empty_bar(stage), kClusterMask);
-          else
-            mma_commit(empty_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
-        mma_commit(tfull_bar(acc));
-      }
-      if (!ok) {  // let issued MMAs finish before TMEM is freed
-        mma_commit(drain_bar);
-        mbar_wait_drain(drain_bar, 0, 200000000ull);
-      }
-    }
-  } else {
-    // ---------------- epilogue ----------------
-    const int ew = warp - 2;          // 0 .. EPI_WARPS-1
-    const int quarter = warp & 3;     // TMEM lanes this warp may access
-    const int col0 = (ew >> 2) * kColsPerWarp;
-    const uint32_t bufs = sC + ew * NBOX * cbox_bytes<BOXW>();
-    float* col_scale = reinterpret_cast<float*>(smem + L::kOffScale) + ew * kColsPerWarp;
-    int it = 0;
-    uint32_t box = 0;
-    for (int tg = group; tg < num_group_tiles; tg += ngroups, ++it) {
-      const TileCoord tc = coord(tg);
-      const int acc = it & 1;
-      const uint32_t acc_par = (it >> 1) & 1;
-      const int m_start = tc.mb * kBM + quarter * 32;
-      const int n_start = tc.nb * BN + col0;
-      float row_scale = 0.f;
-      if constexpr (kScaled) {
-        __syncwarp();
-        for (int i = lane; i < kColsPerWarp; i += 32) {
-          const int n = n_start + i;
-          col_scale[i] = (n < p.N) ? p.b_scale[n] : 0.f;
-        }
-        const int row = m_start + lane;
-        if constexpr (GATHER) {
-          const int32_t v = row < p.M ? p.gather_idx[row] : -1;
-          row_scale = (v >= 0 && v < p.rows_src) ? p.a_scale[v] : 0.f;
-        } else {
-          row_scale = (row < p.M) ? p.a_scale[row] : 0.f;
-        }
-        __syncwarp();
-      }
-      const bool ok = mbar_wait(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             acc * kAccStride + col0;
-      epilogue_tile<kColsPerWarp, kScaled, NBOX, BOXW>(taddr, bufs, box, col_scale, row_scale, &tmC,
-                                                 n_start, m_start, p.N, p.M, lane, [&]() {
-                                                   tc_fence_before();
-                                                   mbar_arrive(tempty_bar(acc));
-                                                 });
-    }
-    if (lane == 0) bulk_wait_group<0>();
-    __syncwarp();
-  }
-
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  if constexpr (CLUSTER > 1) cluster_sync();  // no CTA leaves while a peer may still signal it
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Pair kernel: two CTAs on neighbouring SMs compute one 256 x BN tile with
@@ -386,7 +85,6 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   constexpr uint32_t kTmemCols = 512;
   constexpr int kAccStride = 256;
   constexpr int kColsPerWarp = L::kColsPerWarp;
-  constexpr uint16_t kBoth = 0x3;
   static_assert(BN <= 256 && BN % 64 == 0, "BN");
   static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
 
@@ -523,17 +221,17 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             else
               mma_f8f6f4_pair(d, ad, bd, kIdesc, (kb | k) != 0);
           }
-          mma_commit_pair(empty_bar(stage), kBoth);
+          mma_commit_pair_both(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit_pair(tfull_bar(acc), kBoth);
+        mma_commit_pair_both(tfull_bar(acc));
       }
       if (!ok) {
-        mma_commit_pair(drain_bar, 0x1);
+        mma_commit_pair(drain_bar);
         mbar_wait_drain(drain_bar, 0, 200000000ull);
       }
     }
@@ -590,104 +288,340 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Gather kernel (ptpc): one CTA per SM, persistent over 128 x 256 output tiles;
+// output row m reads source row p.gather_idx[m] of the source A [rows_src][K]
+// and its scale a_scale[gather_idx[m]] (ROCm/aiter PR 6539, Technical Details:
+// the gather_kv_b_proj kernel gathers its A rows inside the GEMM's pipeline).
+// Two warps after the epilogue warps copy the tile's rows into the stage with
+// 16-byte cp.async, eight lanes per row, writing the 128-byte-swizzled layout
+// the MMA reads, and arrive on full[s] as their copies complete; each CTA loads
+// its whole 256-row B tile by TMA (evict-last: every row panel re-reads it).
+// (Gathering with TMA tile::gather4 took 33 copy operations per stage instead
+// of 2 and ran 2.5x slower than the plain GEMM, bound by the TMA unit.)  An
+// index outside [0, rows_src) -- and every row past M -- reads source row 0 and
+// gets scale 0, so no copy leaves the source and such a row's output is zero
+// (or clipped).
+// ---------------------------------------------------------------------------
+
+template <int STAGES, int EPI_WARPS, int NBOX>
+struct GatherLayout {
+  static constexpr int kBN = 256;
+  static constexpr int kAStage = kBM * kRowBytes;
+  static constexpr int kBStage = kBN * kRowBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + STAGES * kAStage;
+  static constexpr int kOffC = kOffB + STAGES * kBStage;
+  static constexpr int kOffScale = kOffC + EPI_WARPS * NBOX * kCBoxBytes;  // per-warp column scales
+  static constexpr int kScaleCols = kBN * 4 / EPI_WARPS;                  // columns per warp
+  static constexpr int kOffBar = kOffScale + EPI_WARPS * kScaleCols * 4;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "alignment");
+  static_assert(kDynSmem <= 232448, "shared memory");
+};
+
+template <int STAGES, int EPI_WARPS, int NBOX>
+__global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
+    gather_gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
+                       const GemmParams p) {
+  using L = GatherLayout<STAGES, EPI_WARPS, NBOX>;
+  constexpr int BN = L::kBN;
+  constexpr int kBK = 128;          // K elements (bytes) per stage
+  constexpr int kUmmaK = 32;        // K per tcgen05.mma
+  constexpr int kKSteps = kBK / kUmmaK;
+  constexpr uint32_t kIdesc = instr_desc(0, 0, kBM, BN);
+  constexpr uint32_t kTx = L::kBStage;  // TMA bytes per stage (A comes from the gather warps)
+  constexpr int kGatherThreads = 64;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr int kAccStride = 256;
+  constexpr int kColsPerWarp = L::kScaleCols;
+  static_assert(EPI_WARPS == 8, "two epilogue warps per TMEM lane quarter");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sA = smem_addr(smem + L::kOffA);
+  const uint32_t sB = smem_addr(smem + L::kOffB);
+  const uint32_t sC = smem_addr(smem + L::kOffC);
+  const uint32_t bar0 = smem_addr(smem + L::kOffBar);
+  auto full_bar = [&](int s) { return bar0 + 8 * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8 * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8 * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8 * (2 * STAGES + 4);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = p.m_blocks * p.n_blocks;
+  auto coord = [&](int t) {
+    TileCoord c;
+    c.mb = t / p.n_blocks;
+    c.nb = t - c.mb * p.n_blocks;
+    return c;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1 + kGatherThreads);  // the producer's arm + each gather thread's copies
+      mbar_init(empty_bar(s), 1);                  // the MMA commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 32 * EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    misc[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&misc[0]), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = misc[0];
+  const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+
+  if (warp >= 2 + EPI_WARPS) {
+    // ---------------- A rows gathered by index (64 threads, cp.async) ----------------
+    const int t = (warp - 2 - EPI_WARPS) * 32 + lane;  // 0 .. 63
+    const int c = t & 7;                                // 16-byte chunk of the row's 128-byte K slice
+    const int r0 = t >> 3;                              // rows r0, r0 + 8, ..., r0 + 120 of the tile
+    // row r0 + 8 i, chunk c, at (r0 + 8 i) * 128 + ((c ^ r0) << 4): every row of
+    // this thread has swizzle phase r0
+    const uint32_t dst0 = r0 * kRowBytes + ((c ^ r0) << 4);
+    const uint8_t* A = static_cast<const uint8_t*>(p.a_src);
+    auto load_rows = [&](int tile, int32_t (&rows)[16]) {
+      const int mb = tile < num_tiles ? coord(tile).mb : 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int m = mb * kBM + r0 + 8 * i;
+        const int32_t v = (tile < num_tiles && m < p.M) ? __ldg(p.gather_idx + m) : 0;
+        rows[i] = (v >= 0 && v < p.rows_src) ? v : 0;
+      }
+    };
+    int32_t next[16];
+    load_rows(blockIdx.x, next);
+    int stage = 0, kstep = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      int32_t rows[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) rows[i] = next[i];
+      load_rows(tile + gridDim.x, next);  // one tile ahead
+      for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
+        if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+          ok = false;
+          break;
+        }
+        if (kstep != p.skip_kstep) {
+          const int kofs = kb * kBK + 16 * c;
+          const uint32_t nbytes = kofs < p.K ? 16u : 0u;  // past K: zeros
+          const int koff = kofs < p.K ? kofs : 0;
+          const uint32_t dst = sA + stage * L::kAStage + dst0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            cp_async_16(dst + i * 8 * kRowBytes, A + static_cast<int64_t>(rows[i]) * p.K + koff, nbytes);
+          cp_async_arrive_noinc(full_bar(stage));
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    cp_async_wait_all();  // this thread's copies land before the CTA can exit
+  } else if (warp == 0) {
+    // ---------------- TMA producer (B) ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmB);
+      const uint64_t keep_b = l2_policy_evict_last();
+      int stage = 0, kstep = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const TileCoord tc = coord(tile);
+        for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          if (kstep != p.skip_kstep) {
+            mbar_arrive_expect_tx(full_bar(stage), kTx);
+            tma_load_2d_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN, full_bar(stage), keep_b);
+            issued |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {  // loads still in flight must land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1) mbar_wait_drain(full_bar(s), (last_par >> s) & 1, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!mbar_wait(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kAccStride;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, wd, kWhereMmaFull)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();  // the gather warps' cp.async data, for the MMA
+          tc_fence_after();
+          const uint32_t a0 = sA + stage * L::kAStage;
+          const uint32_t b0 = sB + stage * L::kBStage;
+#pragma unroll
+          for (int k = 0; k < kKSteps; ++k)
+            mma_f8f6f4(d, kmajor_sw128_desc(a0 + k * kUmmaK), kmajor_sw128_desc(b0 + k * kUmmaK), kIdesc,
+                       (kb | k) != 0);
+          mma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+      }
+      if (!ok) {  // let issued MMAs finish before TMEM is freed
+        mma_commit(drain_bar);
+        mbar_wait_drain(drain_bar, 0, 200000000ull);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 2;          // 0 .. EPI_WARPS-1
+    const int quarter = warp & 3;     // TMEM lanes this warp may access
+    const int col0 = (ew >> 2) * kColsPerWarp;
+    const uint32_t bufs = sC + ew * NBOX * kCBoxBytes;
+    float* col_scale = reinterpret_cast<float*>(smem + L::kOffScale) + ew * kColsPerWarp;
+    int it = 0;
+    uint32_t box = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+      const TileCoord tc = coord(tile);
+      const int acc = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      const int m_start = tc.mb * kBM + quarter * 32;
+      const int n_start = tc.nb * BN + col0;
+      __syncwarp();
+      for (int i = lane; i < kColsPerWarp; i += 32) {
+        const int n = n_start + i;
+        col_scale[i] = (n < p.N) ? p.b_scale[n] : 0.f;
+      }
+      const int row = m_start + lane;
+      const int32_t v = row < p.M ? p.gather_idx[row] : -1;
+      const float row_scale = (v >= 0 && v < p.rows_src) ? p.a_scale[v] : 0.f;
+      __syncwarp();
+      const bool ok = mbar_wait(tfull_bar(acc), acc_par, wd, kWhereEpiTmemFull);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             acc * kAccStride + col0;
+      epilogue_tile<kColsPerWarp, true, NBOX>(taddr, bufs, box, col_scale, row_scale, &tmC, n_start, m_start,
+                                              p.N, p.M, lane, [&]() {
+                                                tc_fence_before();
+                                                mbar_arrive(tempty_bar(acc));
+                                              });
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
 namespace {
 
 constexpr int kDenseBN = 256;
-// Two configurations: a long K loop wants a deep operand ring (4 stages); a
-// short one (K <= 512, at most 4 stages per tile) is bound by the epilogue, so
-// it trades a stage for 8 epilogue warps (two per TMEM lane quarter).
-constexpr int kShortKBlocks = 4;
 
-template <int MODE, int STAGES, int EPI_WARPS, int NBOX, int CLUSTER, int BOXW, bool GATHER = false>
-struct DenseKernel {
-  using L = DenseLayout<kDenseBN, STAGES, EPI_WARPS, NBOX, BOXW>;
-  static constexpr auto fn = dense_gemm_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX, CLUSTER, BOXW, GATHER>;
-  static constexpr int kBoxW = BOXW;
-  static constexpr bool kPair = false;
-  static constexpr int kThreads = 64 + 32 * EPI_WARPS + (GATHER ? 64 : 0);
-  static constexpr int kCluster = CLUSTER;
-  static cudaError_t prepare() {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
-  }
-};
+// One configuration for every K: the pair kernel on 256 x 256 tiles, 5 stages,
+// 8 epilogue warps (two per TMEM lane quarter).  Short K loops (K <= 512, at most
+// 4 stages a tile) are bound by the per-tile epilogue and the shared-memory
+// traffic; the pair MMA stages half of B per CTA, so each SM writes and reads
+// 32 KB of operands a stage instead of 48 KB for a single-CTA 128 x 256 tile.
+constexpr int kDenseStages = 5;
+constexpr int kDenseEpiWarps = 8;
+constexpr int kDenseBoxes = 2;
 
-template <int MODE, int STAGES, int EPI_WARPS, int NBOX>
+template <int MODE>
 struct PairKernel {
-  using L = PairLayout<kDenseBN, STAGES, EPI_WARPS, NBOX>;
-  static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, STAGES, EPI_WARPS, NBOX>;
-  static constexpr int kThreads = 64 + 32 * EPI_WARPS;
-  static constexpr int kCluster = 2;
-  static constexpr int kBoxW = 32;
-  static constexpr bool kPair = true;
+  using L = PairLayout<kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes>;
+  static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes>;
+  static constexpr int kThreads = 64 + 32 * kDenseEpiWarps;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
   }
 };
 
-// Long K: pair MMA (cta_group::2) on 256 x 256 tiles.  Short K: pairs of CTAs on
-// vertically adjacent 128 x 256 tiles that share (multicast) each B tile.
-constexpr int kLongKStages = 5;
-constexpr int kShortKStages = 3;
-template <int MODE>
-using LongK = PairKernel<MODE, kLongKStages, 8, 2>;
-template <int MODE>
-using ShortK = DenseKernel<MODE, kShortKStages, 8, 2, 2, 32>;
-// The gather-GEMM (ptpc): the short-K configuration with A gathered by index;
-// it serves any K (the gathered workload's K is 512).
-using GatherK = DenseKernel<kModePtpc, kShortKStages, 8, 2, 2, 32, true>;
+// The gather-GEMM (ptpc, any K; the gathered workload's K is 512): 3 stages of
+// 48 KB (A 16 KB + the whole B tile 32 KB), 8 epilogue warps.
+constexpr int kGatherStages = 3;
+struct GatherKernel {
+  using L = GatherLayout<kGatherStages, kDenseEpiWarps, kDenseBoxes>;
+  static constexpr auto fn = gather_gemm_kernel<kGatherStages, kDenseEpiWarps, kDenseBoxes>;
+  static constexpr int kThreads = 128 + 32 * kDenseEpiWarps;
+  static cudaError_t prepare() {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+  }
+};
 
 int dense_bk(int mode) { return mode == kModeBf16 ? 64 : 128; }
 
-bool short_k(int mode, int64_t K) { return (K + dense_bk(mode) - 1) / dense_bk(mode) <= kShortKBlocks; }
+bool encode_c(CUtensorMap* tmC, const LaunchArgs& a) {
+  return encode_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols, kCBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
+}
 
-template <typename Kern>
-sg_status_t launch_with(const LaunchArgs& a, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                        const GemmParams& p) {
-  constexpr int cl = Kern::kCluster;
-  constexpr int bw = Kern::kBoxW;
-  constexpr int rows_per_group = Kern::kPair ? 2 * kBM : kBM * cl;
-  CUtensorMap tmC;
-  if (!encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, bw, kCBoxRows,
-                 bw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
-    return SG_ERR_CUDA;
-  const int group_tiles = static_cast<int>((a.M + rows_per_group - 1) / rows_per_group) * p.n_blocks;
-  const int max_groups = a.num_sms / cl;
-  const int groups = group_tiles < max_groups ? group_tiles : max_groups;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(groups * cl, 1, 1);
-  cfg.blockDim = dim3(Kern::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Kern::L::kDynSmem;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, Kern::fn, tmA, tmB, tmC, p);
-  if (e != cudaSuccess) {
-    note_cuda_error(e);
-    cudaGetLastError();  // clear the non-sticky launch error
-    return SG_ERR_CUDA;
-  }
-  return SG_OK;
+sg_status_t launch_error(cudaError_t e) {
+  if (e == cudaSuccess) return SG_OK;
+  note_cuda_error(e);
+  cudaGetLastError();  // clear the non-sticky launch error
+  return SG_ERR_CUDA;
 }
 
 template <int MODE>
 sg_status_t launch_dense_impl(const LaunchArgs& a) {
+  using Kern = PairKernel<MODE>;
   const bool bf16 = (MODE == kModeBf16);
   const int bk = dense_bk(MODE);
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint64_t el = bf16 ? 2 : 1;
-  static_assert(LongK<MODE>::kCluster == ShortK<MODE>::kCluster, "one B tensor map for both");
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC;
   if (!encode_2d(&tmA, dt, a.A, a.K, a.M, a.K * el, bk, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, kDenseBN / LongK<MODE>::kCluster,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, kDenseBN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_c(&tmC, a))
     return SG_ERR_CUDA;
   GemmParams p{};
   p.M = static_cast<int32_t>(a.M);
@@ -702,22 +636,30 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
   p.b_scale = static_cast<const float*>(a.b_scale);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  return short_k(MODE, a.K) ? launch_with<ShortK<MODE>>(a, tmA, tmB, p)
-                            : launch_with<LongK<MODE>>(a, tmA, tmB, p);
-}
-
-template <int MODE>
-cudaError_t prepare_dense() {
-  cudaError_t e = LongK<MODE>::prepare();
-  if (e == cudaSuccess) e = ShortK<MODE>::prepare();
-  if (e == cudaSuccess && MODE == kModePtpc) e = GatherK::prepare();
-  return e;
+  const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
+  const int max_pairs = a.num_sms / 2;
+  const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(Kern::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Kern::L::kDynSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launch_error(cudaLaunchKernelEx(&cfg, Kern::fn, tmA, tmB, tmC, p));
 }
 
 }  // namespace
 
 cudaError_t dense_prepare(int mode) {
-  return mode == kModeBf16 ? prepare_dense<kModeBf16>() : prepare_dense<kModePtpc>();
+  if (mode == kModeBf16) return PairKernel<kModeBf16>::prepare();
+  const cudaError_t e = PairKernel<kModePtpc>::prepare();
+  return e == cudaSuccess ? GatherKernel::prepare() : e;
 }
 
 sg_status_t dense_launch(const LaunchArgs& a) {
@@ -725,9 +667,10 @@ sg_status_t dense_launch(const LaunchArgs& a) {
 }
 
 sg_status_t dense_launch_gather(const LaunchArgs& a) {
-  CUtensorMap tmB;  // A is read by the kernel's gather warps, not by TMA
-  if (!encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kDenseBN / GatherK::kCluster,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+  CUtensorMap tmB, tmC;  // A is read by the kernel's gather warps, not by TMA
+  if (!encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.B, a.K, a.N, a.K, 128, kDenseBN,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_c(&tmC, a))
     return SG_ERR_CUDA;
   GemmParams p{};
   p.M = static_cast<int32_t>(a.M);
@@ -745,15 +688,17 @@ sg_status_t dense_launch_gather(const LaunchArgs& a) {
   p.a_src = a.A;
   p.gather_idx = a.gather_idx;
   p.rows_src = static_cast<int32_t>(a.rows_src);
-  return launch_with<GatherK>(a, tmB, tmB, p);  // (the A map argument is unused)
+  const int ctas = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
+  GatherKernel::fn<<<ctas, GatherKernel::kThreads, GatherKernel::L::kDynSmem, a.stream>>>(tmB, tmC, p);
+  return launch_error(cudaGetLastError());
 }
 
-void dense_config(int mode, int64_t K, TileConfig* c) {
+void dense_config(int mode, int64_t /*K*/, TileConfig* c) {
   c->bm = kBM;
   c->bn = kDenseBN;
   c->bk = dense_bk(mode);
-  c->stages = short_k(mode, K) ? kShortKStages : kLongKStages;
-  c->cluster = 2;  // both paths: pairs (pair MMA for long K, shared B for short K)
+  c->stages = kDenseStages;
+  c->cluster = 2;  // pair MMA (cta_group::2) for every K
   c->rows_per_group = 2 * kBM;
 }
 

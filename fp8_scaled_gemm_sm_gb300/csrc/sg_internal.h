@@ -40,6 +40,32 @@ struct TileConfig {
   int rows_per_group;  // output rows one cluster covers per tile (N block) it takes
 };
 
+// Bytes of the A-side and B-side scale buffers of a launch (the layouts of
+// include/scaled_gemm.h; 0 for bf16).
+inline int64_t scale_bytes_a(int mode, int64_t M, int64_t K) {
+  switch (mode) {
+    case SG_MODE_PTPC: return 4 * M;
+    case SG_MODE_BLOCKSCALE: return 4 * (K / 128) * M;
+    case SG_MODE_MXFP8: return (K / 32) * M;
+  }
+  return 0;
+}
+inline int64_t scale_bytes_b(int mode, int64_t N, int64_t K) {
+  switch (mode) {
+    case SG_MODE_PTPC: return 4 * N;
+    case SG_MODE_BLOCKSCALE: return 4 * ((N + 127) / 128) * (K / 128);
+    case SG_MODE_MXFP8: return (K / 32) * N;
+  }
+  return 0;
+}
+
+// Whether the byte ranges [p, p + pb) and [q, q + qb) share a byte.
+inline bool ranges_overlap(const void* p, int64_t pb, const void* q, int64_t qb) {
+  if (!p || !q || pb <= 0 || qb <= 0) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+  return a < b + static_cast<uintptr_t>(qb) && b < a + static_cast<uintptr_t>(pb);
+}
+
 // Encode a 2D tiled TMA descriptor (inner dimension first).  Returns false if
 // the driver rejects it.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,

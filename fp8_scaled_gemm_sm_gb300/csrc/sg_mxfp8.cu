@@ -231,7 +231,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   constexpr uint32_t kTxPair = 2 * (L::kAStage + L::kBStage + L::kSfA + L::kSfB);  // both CTAs' bytes
   constexpr uint32_t kTmemCols = 512;
   constexpr int kAccStride = 256;
-  constexpr uint16_t kBoth = 0x3;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -376,17 +375,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             mma_mxf8_pair(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k),
                           instr_desc_mx(2 * kBM, BN, k, k), tsa, tsb, (kb | k) != 0);
           }
-          mma_commit_pair(empty_bar(stage), kBoth);
+          mma_commit_pair_both(empty_bar(stage));
           if (++stage == kMxStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit_pair(tfull_bar(acc), kBoth);
+        mma_commit_pair_both(tfull_bar(acc));
       }
       if (!ok) {  // let issued MMAs finish before TMEM is freed
-        mma_commit_pair(drain_bar, 0x1);
+        mma_commit_pair(drain_bar);
         mbar_wait_drain(drain_bar, 0, 200000000ull);
       }
     }

@@ -89,12 +89,10 @@ extern "C" sg_status_t scaled_gemm_launch_noalloc(const void* A, const void* B, 
   if (!A || !B || !a_scale || !b_scale || !C) return reject(SG_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned16(A) || !aligned16(B) || !aligned16(a_scale) || !aligned16(b_scale) || !aligned16(C))
     return reject(SG_ERR_MISALIGNED, "pointer not 16-byte aligned");
-  auto overlap = [](const void* p, int64_t pb, const void* q, int64_t qb) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
-    return a < b + static_cast<uintptr_t>(qb) && b < a + static_cast<uintptr_t>(pb);
-  };
-  if (overlap(C, M * N * 2, A, M * K) || overlap(C, M * N * 2, B, N * K))
+  if (sg::ranges_overlap(C, M * N * 2, A, M * K) || sg::ranges_overlap(C, M * N * 2, B, N * K))
     return reject(SG_ERR_INVALID_ARG, "C overlaps A or B");
+  if (sg::ranges_overlap(C, M * N * 2, a_scale, 4 * M) || sg::ranges_overlap(C, M * N * 2, b_scale, 4 * N))
+    return reject(SG_ERR_INVALID_ARG, "C overlaps a scale buffer");
   // The only scratch this kernel needs is its status record.
   if (kStatusRecordBytes > kNoAllocScratchBytes)
     return reject(SG_ERR_UNSUPPORTED_SHAPE, "launch needs more scratch than the static array holds");

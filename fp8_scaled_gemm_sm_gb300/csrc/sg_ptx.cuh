@@ -133,6 +133,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // L2 eviction priorities for TMA copies: the weight B, which every row panel of
 // the output re-reads, is kept (evict_last); the streamed output C goes first
 // (evict_first), so it does not push B out of L2 on its way to memory.
@@ -161,18 +171,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// Same load, multicast: the box lands at offset `dst` in the shared memory of
-// every CTA of the cluster named in `cta_mask`, and completes the transaction
-// count of the barrier at offset `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                                      int32_t y, uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
 
 // ---- clusters ----------------------------------------------------------------------
 
@@ -450,14 +448,19 @@ __device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
-// Pair commit: arrive on the barrier at offset `bar` in every CTA of `cta_mask`
-// once the pair MMAs this thread issued have completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
+// Pair commit (cta_group::2): arrive once on the mbarrier at `bar` (a shared
+// address of this CTA, or a cluster-window address of the peer's from
+// map_to_cta) when every pair MMA / copy this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Issued by the even CTA of a pair: the same arrival on the barrier at offset
+// `bar` in both CTAs (two commits, each tracking the same pair operations).
+__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
+  mma_commit_pair(bar);
+  mma_commit_pair(map_to_cta(bar, 1));
 }
 
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far
@@ -465,15 +468,6 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// Same, arriving on the barrier at offset `bar` in every CTA of `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
       : "memory");
 }
 

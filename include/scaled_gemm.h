@@ -31,6 +31,7 @@
  *   A        [M][K] row-major (K contiguous): e4m3 bytes, or bf16 in SG_MODE_BF16
  *   B        [N][K] row-major (K contiguous): same element type as A
  *   C        [M][N] row-major bf16 (N contiguous); must not overlap A, B or the scales
+ *            (checked on the host: an overlap returns SG_ERR_INVALID_ARG)
  *   ptpc        a_scale float[M],            b_scale float[N]
  *   blockscale  a_scale float[K/128][M],     b_scale float[ceil(N/128)][K/128]
  *   mxfp8       a_scale uint8[K/32][M],      b_scale uint8[K/32][N]     (e8m0 codes)
@@ -50,7 +51,9 @@
  * such handle from several host threads or streams are safe.  An mxfp8 handle owns
  * a device workspace (its launch first rearranges the scales there for the tensor
  * core), so launches on one mxfp8 handle must be ordered: issue them on one stream,
- * or order their streams, or use one handle per stream.  Destroying a handle must
+ * or order their streams, or use one handle per stream.  (The one departure from a
+ * workspace-free plan: the block-scaled MMA reads its scales from tensor memory in
+ * a layout the K-block-major scale arrays do not have.)  Destroying a handle must
  * not race a launch on it.
  */
 #ifndef SCALED_GEMM_H
@@ -110,19 +113,29 @@ sg_status_t scaled_gemm_launch(sg_handle_t h, const void* A, const void* B, cons
  * A_src e4m3 [R][K] row-major, a_scale_src float[R], idx int32[M] (device
  * pointers, 16-byte aligned, caller-owned); B, b_scale and C as for ptpc.  An index
  * outside [0, R) names no row: that output row is zero (never read out of
- * bounds).  The rows are gathered inside the GEMM's pipeline (TMA tile::gather4),
- * not copied out first.  Shape rules as for ptpc, with 0 <= R < 2^31; R == 0 or
- * K == 0 writes C = 0.  Returns SG_ERR_INVALID_ARG on a plan of another mode.
+ * bounds).  The rows are gathered inside the GEMM's pipeline: two warps of each
+ * CTA copy every stage's rows with cp.async into the swizzled shared-memory tile
+ * the MMA reads; they are never copied out first.  Shape rules as for ptpc, with
+ * 0 <= R < 2^31; R == 0 or K == 0 writes C = 0.  Returns SG_ERR_INVALID_ARG on a plan of another mode.
  * Cited: ROCm/aiter PR 6539, Motivation and Technical Details (gather_kv_b_proj:
  * the KV projection GEMM over rows gathered by index).                            */
 sg_status_t scaled_gemm_launch_gather(sg_handle_t h, const void* A_src, int64_t R, const int32_t* idx,
                                       const void* B, const void* a_scale_src, const void* b_scale,
                                       void* C, int64_t M, sg_stream_t stream);
 
-/* Release the plan.  NULL is accepted.  Must not race a launch on the same handle. */
+/* Release the plan (its status word and, for mxfp8, its workspace).  NULL is
+ * accepted.  Must not race a launch being enqueued on the same handle from another
+ * thread; launches already enqueued may still run (freeing device memory waits for
+ * the device first).  Returns SG_OK,
+ * or SG_ERR_CUDA if freeing device memory failed (the handle is released anyway).
+ * Cited: ROCm/mori PR 809, "Using it" (the op is an instance used inside a
+ * `with` block that releases it at the end) and "Test plan" (close).            */
 sg_status_t scaled_gemm_destroy(sg_handle_t h);
 
-/* A static English description of a status code. */
+/* A static English description of a status code (never NULL; an unknown code
+ * gives "unknown status").  Refusals are returned, not raised, so that a C caller
+ * sees them: ROCm/mori PR 809, "Using it" (operands the launch would misread are
+ * refused with an error; the constructor refuses bad configuration).           */
 const char* scaled_gemm_status_string(sg_status_t s);
 
 /* Tile geometry of a launch at M = M_max: BM x BN output tiles per CTA (BN: the
@@ -130,7 +143,10 @@ const char* scaled_gemm_status_string(sg_status_t s);
  * stage, `stages` shared-memory stages, `grid` persistent CTAs (whole clusters,
  * where the kernel runs CTAs in pairs).  mxfp8 chooses BN per launch from M and N
  * (see scaled_gemm_set_tile), so a smaller M may use the other width.  Any output
- * pointer may be NULL.                                                           */
+ * pointer may be NULL.  Returns SG_ERR_INVALID_ARG for a NULL handle.
+ * Cited: a review of ROCm/mori PR 809, Smaller points (the tile configuration a
+ * kernel serves is validated and reported, and the default should follow the
+ * shape).                                                                        */
 sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int* stages, int* grid);
 
 /* Pin the output-tile width every later launch of the plan uses, or pass 0 to let
@@ -150,14 +166,21 @@ sg_status_t scaled_gemm_set_tile(sg_handle_t h, int bn);
  * SG_OK or SG_ERR_TIMEOUT in *code and, for a timeout, the role / wait site that gave
  * up in *where (0 otherwise).  Every mbarrier wait in the kernels is bounded; on
  * expiry the kernel records the site here, drains its own copies in flight, frees
- * its tensor memory and returns, so the context stays usable.                    */
+ * its tensor memory and returns, so the context stays usable.  Returns
+ * SG_ERR_INVALID_ARG for a NULL handle or code, SG_ERR_CUDA if the copy fails.
+ * Cited: ROCm/mori PR 809, Worth a reviewer's attention (a grid whose blocks all
+ * spin on data that never arrives never finishes): here no wait is unbounded, and
+ * a wait that gives up is reported instead of hanging the stream.               */
 sg_status_t scaled_gemm_debug_status(sg_handle_t h, sg_stream_t stream, int32_t* code,
                                      int32_t* where);
 
 /* Set the time limit of every kernel-side wait for this plan (nanoseconds; 0 = the
  * default, 4 s) and, for tests of the watchdog only, make the producer of every CTA
  * skip its `skip_kstep`-th pipeline stage (-1 = never) so that the consumer's wait
- * expires.  Not for production use.                                              */
+ * expires.  Not for production use.  Returns SG_ERR_INVALID_ARG for a NULL handle,
+ * a negative limit or skip_kstep < -1.  Cited: ROCm/aiter PR 6539, Technical
+ * Details (the races were hunted with fault injection); the fault here is made on
+ * the host's side of the launch, never by corrupting device memory.             */
 sg_status_t scaled_gemm_set_debug(sg_handle_t h, int64_t timeout_ns, int64_t skip_kstep);
 
 /* Element types of the activations given to scaled_gemm_quantize. */

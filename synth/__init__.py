@@ -17,6 +17,8 @@ from .gen import (  # noqa: F401
     paged_indices,
     GATHER_CONFIGS,
     make_int_case,
+    with_extreme_mx_codes,
+    with_wide_block_scales,
     quantize_e4m3_rows,
     quantize_e4m3_blocks_1x128,
     quantize_e4m3_blocks_128x128,

@@ -171,6 +171,48 @@ def make_int_case(M: int, N: int, K: int, lo: int = -16, hi: int = 16, seed: int
     )
 
 
+def with_extreme_mx_codes(case: Case, seed: int = 0, codes=(0, 1, 127, 253, 254)) -> Case:
+    """The same mxfp8 operands with e8m0 scale codes at the ends of the range,
+    mixed per K block: block j of A takes a base code a_j drawn from `codes`, each
+    row of the block a_j + d (d in {-1, 0, 1}, kept in [0, 254]); block j of B
+    takes 254 - a_j + e (e in {-1, 0, 1}, kept in [0, 254]).  Every block's
+    product of scales is then 2^-2 .. 2^2, so all blocks contribute to every
+    output element while the tensor core decodes codes 0, 1, 253 and 254."""
+    assert case.mode == "mxfp8"
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+    kb = case.K // 32
+    base = torch.tensor(codes, dtype=torch.int64)[torch.randint(0, len(codes), (kb,), generator=g)]
+    da = torch.randint(-1, 2, (kb, case.M), generator=g)
+    db = torch.randint(-1, 2, (kb, case.N), generator=g)
+    sa = (base[:, None] + da).clamp(0, 254).to(torch.uint8).contiguous()
+    sb = (254 - base[:, None] + db).clamp(0, 254).to(torch.uint8).contiguous()
+    return dataclasses.replace(case, sa=sa, sb=sb)
+
+
+def with_wide_block_scales(case: Case, seed: int = 0, lo: int = -40, hi: int = 40, zero_frac: float = 0.05) -> Case:
+    """The same blockscale operands with fp32 block scales spread over binades
+    2^lo .. 2^hi (a random significand in [1, 2) times 2^u, u uniform in [lo, hi],
+    random sign), a fraction `zero_frac` of them set to zero, plus one A row and
+    one B block column of scales that are all zero."""
+    assert case.mode == "blockscale"
+    g = torch.Generator("cpu")
+    g.manual_seed(seed)
+
+    def draw(shape):
+        sig = 1.0 + torch.rand(shape, generator=g, dtype=torch.float64)
+        u = torch.randint(lo, hi + 1, shape, generator=g).double()
+        sign = torch.where(torch.rand(shape, generator=g) < 0.5, -1.0, 1.0).double()
+        v = (sign * sig * torch.pow(2.0, u)).float()
+        return torch.where(torch.rand(shape, generator=g) < zero_frac, torch.zeros_like(v), v)
+
+    sa = draw(tuple(case.sa.shape))
+    sb = draw(tuple(case.sb.shape))
+    sa[:, case.M // 2] = 0.0          # one row of A: every block scale zero
+    sb[:, sb.shape[1] // 2] = 0.0     # one K block of B: zero for every N block
+    return dataclasses.replace(case, sa=sa.contiguous(), sb=sb.contiguous())
+
+
 @dataclasses.dataclass
 class GatherCase:
     """One gather-GEMM problem (ptpc): output row i reads row idx[i] of A_src.

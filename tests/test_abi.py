@@ -108,3 +108,14 @@ def test_quantize_rejects_bad_arguments_on_the_host(lib):
     assert f(1, 0, None, 0, 128, None, None, None) == 0        # nothing to do
     assert f(1, 0, None, 4, 128, None, None, None) == 1        # NULL pointers
     assert f(1, 0, 16, 4, 128, 8, 32, None) == 3               # misaligned
+
+
+def test_noalloc_rejects_c_overlapping_a_scale_buffer_on_the_host(lib):
+    # C [16, 256] bf16 occupies 8 KB from 0x300000; any scale buffer inside it is
+    # refused before the library touches the device (addresses are never dereferenced)
+    f = binding.lib().scaled_gemm_launch_noalloc
+    A, B, C = 0x100000, 0x200000, 0x300000
+    assert f(A, B, C + 4096, 0x400000, C, 16, 256, 256, None) == 1      # a_scale inside C
+    assert f(A, B, 0x400000, C + 8192 - 16, C, 16, 256, 256, None) == 1  # b_scale's first bytes inside C
+    assert f(A, B, C - 32, 0x400000, C, 16, 256, 256, None) == 1         # a_scale (64 B) straddles C's start
+    assert f(C, B, 0x400000, 0x500000, C, 16, 256, 256, None) == 1       # A is C

@@ -123,7 +123,9 @@ def test_gather_out_of_range_and_repeated_indices(lib):
 
 
 def test_identity_gather_equals_the_plain_launch_bit_for_bit(lib):
-    # K = 512: both launches run the same (short-K) pipeline, so the outputs agree bitwise
+    # the gather kernel (one CTA per 128 x 256 tile) and the plain launch (the pair
+    # kernel) sum every element over K in the same order of K = 32 MMA steps and
+    # apply the scales alike, so the outputs agree bitwise
     import gpu_util
 
     plain = synth.make_case("ptpc", 384, 512, 512, seed=9, b_std=0.02)
