@@ -70,8 +70,8 @@ __device__ __forceinline__ void regs_inc_promo() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBsRegsPromo));
 }
 
-constexpr int kBpStages = 6;
-constexpr int kBpBoxes = 2;  // C store boxes per promotion warp
+constexpr int kBpStages = 5;
+constexpr int kBpBoxes = kBsCols / 32;  // C store boxes per promotion warp: its whole 32-row strip
 
 struct BpLayout {
   static constexpr int kAStage = kBM * kRowBytes;
@@ -247,7 +247,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const int kblocks = p.k_blocks;
     const int nsb = (p.N + 127) / 128;  // B scale blocks along N
     int part = 0;
-    uint32_t ppar = 0, box = 0;
+    uint32_t ppar = 0;
     bool ok = true;
     // Scale products s = sa[j][row] * sb[n/128][j] are loaded kScaleAhead K blocks
     // before they are needed (a ring of registers), and the first ones of the next
@@ -337,8 +337,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
       }
       const int n_start = tc.nb * kBsBN + col0;
+      // the strip's boxes were last read by the previous tile's stores
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
 #pragma unroll
-      for (int h = 0; h < kBsCols / 32; ++h) {
+      for (int h = 0; h < kBpBoxes; ++h) {
         uint32_t packed[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -346,8 +349,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           unpack_f32x2(acc[16 * h + j], lo, hi);
           packed[j] = pack_bf16x2(lo, hi);
         }
-        store_box32<kBpBoxes>(bufs, box, packed, &tmC, n_start + 32 * h, m_start, p.N, p.M, lane);
+        stage_box32(bufs + h * kCBoxBytes, packed, lane);
       }
+      store_staged_box32<kBpBoxes>(bufs, &tmC, n_start, m_start, p.N, p.M, lane);
     }
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();

@@ -52,7 +52,7 @@ namespace sg {
 // on its tmem_empty[acc].  Each CTA reads its own 128 accumulator rows.
 // ---------------------------------------------------------------------------
 
-template <int BN, int STAGES, int EPI_WARPS, int NBOX>
+template <int BN, int STAGES, int EPI_WARPS, int NBOX, int BOXW>
 struct PairLayout {
   static constexpr int kAStage = kBM * kRowBytes;
   static constexpr int kBStage = (BN / 2) * kRowBytes;
@@ -60,21 +60,22 @@ struct PairLayout {
   static constexpr int kOffB = kOffA + STAGES * kAStage;
   static constexpr int kOffC = kOffB + STAGES * kBStage;
   static constexpr int kColsPerWarp = BN * 4 / EPI_WARPS;
-  static constexpr int kOffScale = kOffC + EPI_WARPS * NBOX * kCBoxBytes;
+  static constexpr int kOffScale = kOffC + EPI_WARPS * NBOX * cbox_bytes<BOXW>();
   static constexpr int kOffBar = kOffScale + EPI_WARPS * kColsPerWarp * 4;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 4 * STAGES;
   static constexpr int kDynSmem = kBytes + 1024;
   static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "alignment");
+  static_assert(kDynSmem <= 232448, "shared memory");
 };
 
-template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX>
+template <int MODE, int BN, int STAGES, int EPI_WARPS, int NBOX, int BOXW>
 __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     dense_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using L = PairLayout<BN, STAGES, EPI_WARPS, NBOX>;
+  using L = PairLayout<BN, STAGES, EPI_WARPS, NBOX, BOXW>;
   constexpr bool kScaled = (MODE == kModePtpc);
   constexpr int kBK = (MODE == kModeBf16) ? 64 : 128;
   constexpr int kUmmaK = (MODE == kModeBf16) ? 16 : 32;
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   constexpr int kAccStride = 256;
   constexpr int kColsPerWarp = L::kColsPerWarp;
   static_assert(BN <= 256 && BN % 64 == 0, "BN");
-  static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+  static_assert(EPI_WARPS == 8 || EPI_WARPS == 16, "epilogue warps");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int col0 = (ew >> 2) * kColsPerWarp;
-    const uint32_t bufs = sC + ew * NBOX * kCBoxBytes;
+    const uint32_t bufs = sC + ew * NBOX * cbox_bytes<BOXW>();
     float* col_scale = reinterpret_cast<float*>(smem + L::kOffScale) + ew * kColsPerWarp;
     int it = 0;
     uint32_t box = 0;
@@ -267,8 +268,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              acc * kAccStride + col0;
       const uint32_t release_bar = map_to_cta(tempty_bar(acc), 0);
-      epilogue_tile<kColsPerWarp, kScaled, NBOX>(taddr, bufs, box, col_scale, row_scale, &tmC,
-                                                 n_start, m_start, p.N, p.M, lane, [&]() {
+      epilogue_tile<kColsPerWarp, kScaled, NBOX, BOXW>(taddr, bufs, box, col_scale, row_scale, &tmC,
+                                                       n_start, m_start, p.N, p.M, lane, [&]() {
                                                    tc_fence_before();
                                                    mbar_arrive_cluster_relaxed(release_bar);
                                                  });
@@ -567,18 +568,20 @@ namespace {
 constexpr int kDenseBN = 256;
 
 // One configuration for every K: the pair kernel on 256 x 256 tiles, 5 stages,
-// 8 epilogue warps (two per TMEM lane quarter).  Short K loops (K <= 512, at most
-// 4 stages a tile) are bound by the per-tile epilogue and the shared-memory
-// traffic; the pair MMA stages half of B per CTA, so each SM writes and reads
-// 32 KB of operands a stage instead of 48 KB for a single-CTA 128 x 256 tile.
+// 16 epilogue warps (four per TMEM lane quarter, 64 columns each, one 32 x 32
+// store box each).  Short K loops (K <= 512, at most 4 stages a tile) are bound
+// by the per-tile epilogue: a warp's chain of TMEM loads, conversion, staging
+// and TMA stores; four warps per quarter instead of two cut K = 512 from 64 to
+// 53 us at 16384 x 7168 and leave long K unchanged.
 constexpr int kDenseStages = 5;
-constexpr int kDenseEpiWarps = 8;
-constexpr int kDenseBoxes = 2;
+constexpr int kDenseEpiWarps = 16;
+constexpr int kDenseBoxes = 1;
+constexpr int kDenseBoxW = 32;  // columns of a warp's C store box (32: 64-byte swizzle, 64: 128-byte)
 
 template <int MODE>
 struct PairKernel {
-  using L = PairLayout<kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes>;
-  static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes>;
+  using L = PairLayout<kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes, kDenseBoxW>;
+  static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes, kDenseBoxW>;
   static constexpr int kThreads = 64 + 32 * kDenseEpiWarps;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
@@ -588,10 +591,12 @@ struct PairKernel {
 // The gather-GEMM (ptpc, any K; the gathered workload's K is 512): 3 stages of
 // 48 KB (A 16 KB + the whole B tile 32 KB), 8 epilogue warps.
 constexpr int kGatherStages = 3;
+constexpr int kGatherEpiWarps = 8;
+constexpr int kGatherBoxes = 2;
 struct GatherKernel {
-  using L = GatherLayout<kGatherStages, kDenseEpiWarps, kDenseBoxes>;
-  static constexpr auto fn = gather_gemm_kernel<kGatherStages, kDenseEpiWarps, kDenseBoxes>;
-  static constexpr int kThreads = 128 + 32 * kDenseEpiWarps;
+  using L = GatherLayout<kGatherStages, kGatherEpiWarps, kGatherBoxes>;
+  static constexpr auto fn = gather_gemm_kernel<kGatherStages, kGatherEpiWarps, kGatherBoxes>;
+  static constexpr int kThreads = 128 + 32 * kGatherEpiWarps;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
   }
@@ -599,9 +604,9 @@ struct GatherKernel {
 
 int dense_bk(int mode) { return mode == kModeBf16 ? 64 : 128; }
 
-bool encode_c(CUtensorMap* tmC, const LaunchArgs& a) {
-  return encode_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, kCBoxCols, kCBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_64B);
+bool encode_c(CUtensorMap* tmC, const LaunchArgs& a, int box_cols = kCBoxCols) {
+  return encode_2d(tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.C, a.N, a.M, a.N * 2, box_cols, kCBoxRows,
+                   box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 sg_status_t launch_error(cudaError_t e) {
@@ -621,7 +626,7 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
   CUtensorMap tmA, tmB, tmC;
   if (!encode_2d(&tmA, dt, a.A, a.K, a.M, a.K * el, bk, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, kDenseBN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_c(&tmC, a))
+      !encode_c(&tmC, a, kDenseBoxW))
     return SG_ERR_CUDA;
   GemmParams p{};
   p.M = static_cast<int32_t>(a.M);

@@ -67,14 +67,21 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Longest time (ns) one try_wait may keep a waiting thread suspended before it
+// returns false.  A thread suspended in try_wait wakes as soon as the phase
+// completes; without the hint the waiting warps poll the barrier word in a
+// tight loop, and that polling slowed the barriers' producers and consumers
+// (mxfp8 at 32768 x 7168 x 1792: 360 -> 328 us with the hint).
+constexpr uint32_t kSuspendNs = 10000;
+
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return done != 0;
 }
@@ -86,15 +93,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
                                           int where) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  uint32_t spins = 0;
   while (true) {
     if (mbar_test(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
-      if (*wd.abort) return false;
-      if (global_timer_ns() - t0 > wd.timeout_ns) {
-        record_timeout(wd, where);
-        return false;
-      }
+    if (*wd.abort) return false;
+    if (global_timer_ns() - t0 > wd.timeout_ns) {
+      record_timeout(wd, where);
+      return false;
     }
   }
 }
@@ -215,10 +219,10 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return done != 0;
 }
@@ -227,15 +231,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   int where) {
   if (mbar_test_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  uint32_t spins = 0;
   while (true) {
     if (mbar_test_cluster(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
-      if (*wd.abort) return false;
-      if (global_timer_ns() - t0 > wd.timeout_ns) {
-        record_timeout(wd, where);
-        return false;
-      }
+    if (*wd.abort) return false;
+    if (global_timer_ns() - t0 > wd.timeout_ns) {
+      record_timeout(wd, where);
+      return false;
     }
   }
 }
@@ -456,11 +457,16 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
                : "memory");
 }
 
-// Issued by the even CTA of a pair: the same arrival on the barrier at offset
-// `bar` in both CTAs (two commits, each tracking the same pair operations).
+// Issued by the even CTA of a pair: one commit whose arrival reaches the barrier
+// at offset `bar` in both CTAs of the pair.  (This is an mbarrier signal, not a
+// memory access: no TMA load in this library is multicast.  One commit instead of
+// a commit per CTA saves a tcgen05 instruction per stage on the MMA thread, whose
+// issue rate the scale-copying kernels are bound by: mxfp8 325 -> 307 us.)
 __device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
-  mma_commit_pair(bar);
-  mma_commit_pair(map_to_cta(bar, 1));
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(0x3))
+      : "memory");
 }
 
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so far
