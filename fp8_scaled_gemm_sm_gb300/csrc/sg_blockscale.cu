@@ -80,7 +80,7 @@ struct BpLayout {
   static constexpr int kOffB = kOffA + kBpStages * kAStage;
   static constexpr int kOffC = kOffB + kBpStages * kBStage;
   static constexpr int kOffBar = kOffC + kBsWarps * kBpBoxes * kCBoxBytes;
-  static constexpr int kNumBars = 2 * kBpStages + 2 * kBsParts + 1;
+  static constexpr int kNumBars = 2 * kBpStages + 2 * kBsParts + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16 + 4 * kBpStages;
   static constexpr int kDynSmem = kBytes + 1024;
@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   auto pfull_bar = [&](int q) { return bar0 + 8 * (2 * kBpStages + q); };
   auto pempty_bar = [&](int q) { return bar0 + 8 * (2 * kBpStages + kBsParts + q); };
   const uint32_t drain_bar = bar0 + 8 * (2 * kBpStages + 2 * kBsParts);
+  const uint32_t cstaged_bar = drain_bar + 8;  // every promotion warp staged its strip of C
+  const uint32_t cfree_bar = drain_bar + 16;   // the store warp's stores have read the strips
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   uint32_t* last_par = misc + 4;
 
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       mbar_init(pempty_bar(q), 2 * kBsWarps);  // one elected lane per promotion warp of both CTAs
     }
     mbar_init(drain_bar, 1);
+    mbar_init(cstaged_bar, kBsWarps);
+    mbar_init(cfree_bar, 1);
     misc[1] = 0;
     fence_mbarrier_init();
   }
@@ -200,11 +204,40 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         for (int s = 0; s < kBpStages; ++s)
           if ((issued >> s) & 1) mbar_wait_drain(empty_bar(s), last_par[s], 200000000ull);
       }
+    } else if (warp == 2 && lane == 0) {
+      // ---------------- C store issuer ----------------
+      // The promotion warps stage a tile's output in shared memory and fence it;
+      // this thread issues the tile's 32 TMA stores, so the promotion warps never
+      // block on the TMA unit's queue (stores issued by them stalled the partial
+      // pipeline at every tile end: 243 -> 224 us without them).
+      tma_prefetch_desc(&tmC);
+      const uint64_t pol = l2_policy_evict_first();
+      uint32_t tpar = 0;
+      for (int tp = pair; tp < num_pair_tiles; tp += npairs) {
+        const TileCoord tc = coord(tp);
+        if (!mbar_wait(cstaged_bar, tpar, wd, kWhereEpiTmemFull)) break;
+        tpar ^= 1;
+#pragma unroll 1
+        for (int ew = 0; ew < kBsWarps; ++ew) {
+          const int y = tc.mb * kBM + (ew & 3) * 32;
+#pragma unroll
+          for (int h = 0; h < kBpBoxes; ++h) {
+            const int x = tc.nb * kBsBN + (ew >> 2) * kBsCols + 32 * h;
+            if (x < p.N && y < p.M)
+              tma_store_2d_hint(&tmC, sC + (ew * kBpBoxes + h) * kCBoxBytes, x, y, pol);
+          }
+        }
+        bulk_commit_group();
+        bulk_wait_group_read<0>();
+        mbar_arrive(cfree_bar);
+      }
+      bulk_wait_group<0>();
     } else if (warp == 1 && lane == 0 && leader) {
       // ---------------- pair MMA issuer: one TMEM partial per K block ----------------
       int stage = 0, part = 0;
       uint32_t phase = 0, ppar = 0;
       bool ok = true;
+      const uint64_t desc_a = kmajor_sw128_desc(sA), desc_b = kmajor_sw128_desc(sB);
       for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait_cluster(pempty_bar(part), ppar ^ 1, wd, kWhereMmaTmemEmpty) ||
@@ -214,11 +247,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           }
           tc_fence_after();
           const uint32_t d = tmem_base + part * kBsBN;
-          const uint32_t a0 = sA + stage * L::kAStage;
-          const uint32_t b0 = sB + stage * L::kBStage;
+          const uint64_t da = desc_advance(desc_a, stage * L::kAStage);
+          const uint64_t db = desc_advance(desc_b, stage * L::kBStage);
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k)
-            mma_f8f6f4_pair(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k), kIdesc, k != 0);
+            mma_f8f6f4_pair(d, desc_advance(da, 32 * k), desc_advance(db, 32 * k), kIdesc, k != 0);
           mma_commit_pair_both(empty_bar(stage));
           mma_commit_pair_both(pfull_bar(part));
           if (++stage == kBpStages) {
@@ -247,12 +280,15 @@ __global__ void __launch_bounds__(kBsThreads, 1)
     const int kblocks = p.k_blocks;
     const int nsb = (p.N + 127) / 128;  // B scale blocks along N
     int part = 0;
-    uint32_t ppar = 0;
+    uint32_t ppar = 0, cpar = 1;  // cfree: a fresh barrier counts as freed
     bool ok = true;
     // Scale products s = sa[j][row] * sb[n/128][j] are loaded kScaleAhead K blocks
-    // before they are needed (a ring of registers), and the first ones of the next
-    // tile are loaded before this tile's epilogue, so no promotion step waits on
-    // a global load.  The accumulator is 64 packed fp32 pairs, updated with one
+    // before they are needed (a ring of registers).  When the K-block count is a
+    // multiple of the ring, the next tile's first kScaleAhead scales are loaded
+    // during this tile's last kScaleAhead K blocks (into the slots they free), so
+    // the first promotion of a tile does not wait on a load issued at its start
+    // (that wait cost about 4000 cycles a tile); otherwise they are loaded before
+    // the epilogue.  The accumulator is 64 packed fp32 pairs, updated with one
     // f32x2 FMA per pair.
     constexpr int kScaleAhead = 4;
     float ring_a[kScaleAhead], ring_b[kScaleAhead];
@@ -281,9 +317,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       for (int d = 0; d < kScaleAhead; ++d)
         if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
     }
+    const bool ring_wraps = kblocks % kScaleAhead == 0;
     for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
-      const TileCoord tc = coord(tp);
-      const int m_start = tc.mb * kBM + quarter * 32;
+      const int tn = tp + npairs;
       uint64_t acc[kBsCols / 2];
 #pragma unroll
       for (int j = 0; j < kBsCols / 2; ++j) acc[j] = 0;
@@ -294,7 +330,13 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           if (kb < kblocks) {
             const float sc = ring_a[d] * ring_b[d];
             const uint64_t s2 = pack_f32x2(__float_as_uint(sc), __float_as_uint(sc));
-            if (kb + kScaleAhead < kblocks) load_scales(kb + kScaleAhead, ring_a[d], ring_b[d]);
+            if (kb + kScaleAhead < kblocks) {
+              load_scales(kb + kScaleAhead, ring_a[d], ring_b[d]);
+            } else if (ring_wraps && tn < num_pair_tiles) {
+              // slot d next holds K block kb + kScaleAhead - kblocks (= d) of the next tile
+              if (kb + kScaleAhead == kblocks) tile_scale_ptrs(tn);
+              load_scales(kb + kScaleAhead - kblocks, ring_a[d], ring_b[d]);
+            }
             ok = mbar_wait_cluster(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
             if (!__all_sync(0xffffffffu, ok)) {
               ok = false;
@@ -328,18 +370,17 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
       }
       if (!ok) break;
-      // the next tile's first scales load while this tile is stored
-      const int tn = tp + npairs;
-      if (tn < num_pair_tiles) {
+      // otherwise the next tile's first scales load while this tile is stored
+      if (!ring_wraps && tn < num_pair_tiles) {
         tile_scale_ptrs(tn);
 #pragma unroll
         for (int d = 0; d < kScaleAhead; ++d)
           if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
       }
-      const int n_start = tc.nb * kBsBN + col0;
       // the strip's boxes were last read by the previous tile's stores
-      if (lane == 0) bulk_wait_group_read<0>();
-      __syncwarp();
+      ok = mbar_wait(cfree_bar, cpar, wd, kWhereEpiTmemFull);
+      cpar ^= 1;
+      if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll
       for (int h = 0; h < kBpBoxes; ++h) {
         uint32_t packed[16];
@@ -351,10 +392,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
         }
         stage_box32(bufs + h * kCBoxBytes, packed, lane);
       }
-      store_staged_box32<kBpBoxes>(bufs, &tmC, n_start, m_start, p.N, p.M, lane);
+      fence_proxy_async_smem();  // every writer, before the store warp's TMA stores read it
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cstaged_bar);
     }
-    if (lane == 0) bulk_wait_group<0>();
-    __syncwarp();
   }
 
   __syncwarp();

@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const uint64_t desc_a = kmajor_sw128_desc(sA), desc_b = kmajor_sw128_desc(sB);
       for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
@@ -211,12 +212,12 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = sA + stage * L::kAStage;
-          const uint32_t b0 = sB + stage * L::kBStage;
+          const uint64_t da = desc_advance(desc_a, stage * L::kAStage);
+          const uint64_t db = desc_advance(desc_b, stage * L::kBStage);
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k) {
-            const uint64_t ad = kmajor_sw128_desc(a0 + k * kUmmaK * (kRowBytes / kBK));
-            const uint64_t bd = kmajor_sw128_desc(b0 + k * kUmmaK * (kRowBytes / kBK));
+            const uint64_t ad = desc_advance(da, k * kUmmaK * (kRowBytes / kBK));
+            const uint64_t bd = desc_advance(db, k * kUmmaK * (kRowBytes / kBK));
             if constexpr (MODE == kModeBf16)
               mma_f16_pair(d, ad, bd, kIdesc, (kb | k) != 0);
             else
@@ -475,6 +476,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const uint64_t desc_a = kmajor_sw128_desc(sA), desc_b = kmajor_sw128_desc(sB);
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
@@ -491,12 +493,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
           }
           fence_proxy_async_smem();  // the gather warps' cp.async data, for the MMA
           tc_fence_after();
-          const uint32_t a0 = sA + stage * L::kAStage;
-          const uint32_t b0 = sB + stage * L::kBStage;
+          const uint64_t da = desc_advance(desc_a, stage * L::kAStage);
+          const uint64_t db = desc_advance(desc_b, stage * L::kBStage);
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k)
-            mma_f8f6f4(d, kmajor_sw128_desc(a0 + k * kUmmaK), kmajor_sw128_desc(b0 + k * kUmmaK), kIdesc,
-                       (kb | k) != 0);
+            mma_f8f6f4(d, desc_advance(da, k * kUmmaK), desc_advance(db, k * kUmmaK), kIdesc, (kb | k) != 0);
           mma_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;

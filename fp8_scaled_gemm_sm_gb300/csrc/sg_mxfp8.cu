@@ -346,6 +346,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const uint64_t desc_a = kmajor_sw128_desc(sA), desc_b = kmajor_sw128_desc(sB);
+      const uint64_t desc_sfa = rec_desc(sSfA);
+      const uint64_t desc_sfb = T::kWide ? smem_desc(sSfB, 128, 256, 0) : rec_desc(sSfB);
       for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
@@ -363,16 +366,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           tc_fence_after();
           const uint32_t tsa = tmem_base + sf_col_a<BN>(stage);
           const uint32_t tsb = tmem_base + sf_col_b<BN>(stage);
-          tmem_cp_pair_32x128b_x4(tsa, rec_desc(sSfA + stage * L::kSfA));
+          tmem_cp_pair_32x128b_x4(tsa, desc_advance(desc_sfa, stage * L::kSfA));
           if constexpr (T::kWide)
-            tmem_cp_pair_128x256b(tsb, smem_desc(sSfB + stage * L::kSfB, 128, 256, 0));
+            tmem_cp_pair_128x256b(tsb, desc_advance(desc_sfb, stage * L::kSfB));
           else
-            tmem_cp_pair_32x128b_x4(tsb, rec_desc(sSfB + stage * L::kSfB));
-          const uint32_t a0 = sA + stage * L::kAStage;
-          const uint32_t b0 = sB + stage * L::kBStage;
+            tmem_cp_pair_32x128b_x4(tsb, desc_advance(desc_sfb, stage * L::kSfB));
+          const uint64_t da = desc_advance(desc_a, stage * L::kAStage);
+          const uint64_t db = desc_advance(desc_b, stage * L::kBStage);
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k) {
-            mma_mxf8_pair(d, kmajor_sw128_desc(a0 + 32 * k), kmajor_sw128_desc(b0 + 32 * k),
+            mma_mxf8_pair(d, desc_advance(da, 32 * k), desc_advance(db, 32 * k),
                           instr_desc_mx(2 * kBM, BN, k, k), tsa, tsb, (kb | k) != 0);
           }
           mma_commit_pair_both(empty_bar(stage));

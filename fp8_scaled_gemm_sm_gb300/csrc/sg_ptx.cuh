@@ -371,6 +371,14 @@ __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t addr) {
   return smem_desc(addr, 16, 1024, 2);
 }
 
+// The descriptor of a tile `bytes` further along in shared memory: the start
+// address field (bits 0-13) holds addr >> 4 and every shared address is below
+// 2^18, so the sum never carries out of the field.  Lets the MMA thread step
+// from a stage's base descriptor with one add instead of rebuilding it.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 / kind::f8f6f4 with fp32 accumulation,
 // both operands K-major.  a_fmt / b_fmt: kind::f8f6f4 0 = e4m3; kind::f16 1 = bf16.
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt, int M, int N) {
