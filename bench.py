@@ -265,11 +265,14 @@ def choose_peak(clk):
 GRAPH_MAX_US = 100.0
 
 
-def graph_per_call(launch_fn, stream, calls=200, batches=9):
+def graph_per_call(launch_fn, stream, calls=200, batches=9, gpu_index=None):
     """Median device time per call over `batches` replays of a CUDA graph of
     `calls` back-to-back launches on the same operands (deepseek-ai/DeepGEMM PR
     453, Performance Overhead: CUDA-graph median per call over 9 x 200 calls).
-    The operands stay in L2 between calls where they fit."""
+    The operands stay in L2 between calls where they fit.  With `gpu_index`, the
+    SM clock and throttle reasons sampled during the replays come back too (the
+    replays follow the timed steps, so the clocks there may have dropped)."""
+    clocks = None
     try:
         with torch.cuda.stream(stream):
             launch_fn()
@@ -282,6 +285,9 @@ def graph_per_call(launch_fn, stream, calls=200, batches=9):
             g.replay()
         torch.cuda.synchronize()
         per = []
+        if gpu_index is not None:
+            clocks = ClockSampler(gpu_index)
+            clocks.start()
         for _ in range(batches):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
@@ -291,10 +297,18 @@ def graph_per_call(launch_fn, stream, calls=200, batches=9):
             torch.cuda.synchronize()
             per.append(1e3 * e0.elapsed_time(e1) / calls)
         del g
-        return {"us_median": round(statistics.median(per), 2), "us_min": round(min(per), 2),
-                "calls": calls, "batches": batches}
+        out = {"us_median": round(statistics.median(per), 2), "us_min": round(min(per), 2),
+               "calls": calls, "batches": batches}
+        if clocks is not None:
+            clk = clocks.stop()
+            clocks = None
+            out["clocks"] = {"sm_mhz": clk["sm_mhz"], "reasons": clk["reasons"]}
+        return out
     except RuntimeError as e:
         return {"error": str(e)[:200]}
+    finally:
+        if clocks is not None:
+            clocks.stop()
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -449,7 +463,7 @@ def run_gpu(args, control, rank, local):
     if not args.no_graph:
         for d in work:
             if per[d["name"]]["us"] < GRAPH_MAX_US:
-                per[d["name"]]["graph"] = graph_per_call(lambda d=d: launch(d), stream)
+                per[d["name"]]["graph"] = graph_per_call(lambda d=d: launch(d), stream, gpu_index=local)
 
     quant = None if args.no_quant else run_quantize(binding, dev, stream, hbm)
     extra = None if (args.no_quant or args.only) else run_extra(binding, dev, stream, local, fp8_peak_burst)

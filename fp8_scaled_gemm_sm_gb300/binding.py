@@ -186,8 +186,8 @@ class ScaledGemm:
         return scaled_gemm_get_config(self.handle)
 
     def set_tile(self, bn=0):
-        """Pin the output-tile width of later calls (mxfp8: 224 or 128), or 0 to let
-        each call choose from its M."""
+        """Pin the output-tile width of later calls (mxfp8: 224 or 128; ptpc and
+        bf16: 256 or 128; blockscale: 256), or 0 to let each call choose from its M."""
         scaled_gemm_set_tile(self.handle, bn)
 
     def __call__(self, A, B, a_scale=None, b_scale=None, out=None, stream=None):

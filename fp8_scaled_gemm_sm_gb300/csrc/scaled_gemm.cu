@@ -208,7 +208,7 @@ sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int
   sg::TileConfig c{};
   switch (h->mode) {
     case SG_MODE_BF16:
-    case SG_MODE_PTPC: sg::dense_config(h->mode, h->K, &c); break;
+    case SG_MODE_PTPC: sg::dense_config(h->mode, h->M_max, h->N, h->num_sms, h->tile_bn, &c); break;
     case SG_MODE_MXFP8: sg::mxfp8_config(h->M_max, h->N, h->num_sms, h->tile_bn, &c); break;
     case SG_MODE_BLOCKSCALE: sg::blockscale_config(&c); break;
   }
@@ -235,7 +235,7 @@ sg_status_t scaled_gemm_set_tile(sg_handle_t h, int bn) {
   switch (h->mode) {
     case SG_MODE_MXFP8: ok = sg::mxfp8_tile_ok(bn); break;
     case SG_MODE_BF16:
-    case SG_MODE_PTPC: sg::dense_config(h->mode, h->K, &c); ok = bn == c.bn; break;
+    case SG_MODE_PTPC: ok = sg::dense_tile_ok(bn); break;
     case SG_MODE_BLOCKSCALE: sg::blockscale_config(&c); ok = bn == c.bn; break;
   }
   if (!ok) return fail(SG_ERR_INVALID_ARG, "set_tile: a width this mode does not have");

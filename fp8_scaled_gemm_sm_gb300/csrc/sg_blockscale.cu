@@ -156,6 +156,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  grid_dep_launch();
+  grid_dep_wait();  // no global memory is touched before this point
 
   if (warp < 4) {
     regs_dec_ctl();
@@ -440,19 +442,8 @@ sg_status_t blockscale_launch(const LaunchArgs& a) {
   const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
   const int max_pairs = a.num_sms / 2;
   const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(kBsThreads, 1, 1);
-  cfg.dynamicSmemBytes = BpLayout::kDynSmem;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, blockscale_pair_kernel, tmA, tmB, tmC, p);
+  GemmLaunch l(dim3(2 * pairs), dim3(kBsThreads), BpLayout::kDynSmem, a.stream, 2);
+  const cudaError_t e = cudaLaunchKernelEx(&l.cfg, blockscale_pair_kernel, tmA, tmB, tmC, p);
   if (e != cudaSuccess) {
     note_cuda_error(e);
     cudaGetLastError();  // clear the non-sticky launch error

@@ -87,37 +87,16 @@ __device__ __forceinline__ void store_box(uint32_t bufs, uint32_t& box, const ui
   }
 }
 
-template <int NBOX = 2>
-__device__ __forceinline__ void store_box32(uint32_t bufs, uint32_t& box, const uint32_t (&packed)[16],
-                                            const CUtensorMap* tmC, int x, int y, int N, int M,
-                                            int lane) {
-  store_box<NBOX, 32>(bufs, box, packed, tmC, x, y, N, M, lane);
-}
-
-// One-shot staging of a warp's 32-row strip: NB boxes of 32 columns, written
-// to NB store boxes at `bufs` that no earlier store still reads (the caller
-// waits for that once, before the first stage_box32), then one fence by every
-// writer and NB TMA stores issued back to back by lane 0 (deepseek-ai/DeepGEMM
+// Write one 32 x 32 bf16 box (16 packed pairs per lane, lane = row) into a store
+// box at `buf`, in the 64-byte-swizzled layout of the C tensor map.  The caller
+// has waited until no TMA store still reads the box, and fences the async proxy
+// from every writing thread before a store is issued on it (deepseek-ai/DeepGEMM
 // PR 453, Fix: the fence is executed by all threads, not only the issuing one).
 __device__ __forceinline__ void stage_box32(uint32_t buf, const uint32_t (&packed)[16], int lane) {
 #pragma unroll
   for (int k = 0; k < 4; ++k)
     st_shared_v4(cbox_chunk_addr<32>(buf, lane, k), packed[4 * k], packed[4 * k + 1], packed[4 * k + 2],
                  packed[4 * k + 3]);
-}
-
-template <int NB>
-__device__ __forceinline__ void store_staged_box32(uint32_t bufs, const CUtensorMap* tmC, int x0, int y, int N,
-                                                   int M, int lane) {
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    const uint64_t pol = l2_policy_evict_first();
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-      if (x0 + 32 * b < N && y < M) tma_store_2d_hint(tmC, bufs + b * kCBoxBytes, x0 + 32 * b, y, pol);
-    bulk_commit_group();
-  }
 }
 
 // bf16-round 32 fp32 values (given as bit patterns) into 16 packed pairs.

@@ -142,13 +142,19 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  grid_dep_launch();
+  grid_dep_wait();  // no global memory is touched before this point
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      // L2 priorities: the B panels (every row panel re-reads them) are kept,
+      // an A block goes first once the pairs working on its row panel have
+      // read it; with A at the normal priority it pushed part of B out.
       const uint64_t keep_b = l2_policy_evict_last();
+      const uint64_t drop_a = l2_policy_evict_first();
       int stage = 0, kstep = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
           if (kstep != p.skip_kstep) {
             const uint32_t fb = map_to_cta(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
-            tma_load_2d_pair(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb);
+            tma_load_2d_pair_hint(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb, drop_a);
             tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN + rank * (BN / 2), fb,
                                   keep_b);
             issued |= 1u << stage;
@@ -387,6 +393,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  grid_dep_launch();
+  grid_dep_wait();  // no global memory is touched before this point
 
   if (warp >= 2 + EPI_WARPS) {
     // ---------------- A rows gathered by index (64 threads, cp.async) ----------------
@@ -567,27 +575,51 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 namespace {
 
 constexpr int kDenseBN = 256;
+constexpr int kDenseBNarrow = 128;
 
 // One configuration for every K: the pair kernel on 256 x 256 tiles, 5 stages,
 // 16 epilogue warps (four per TMEM lane quarter, 64 columns each, one 32 x 32
 // store box each).  Short K loops (K <= 512, at most 4 stages a tile) are bound
 // by the per-tile epilogue: a warp's chain of TMEM loads, conversion, staging
 // and TMA stores; four warps per quarter instead of two cut K = 512 from 64 to
-// 53 us at 16384 x 7168 and leave long K unchanged.
+// 53 us at 16384 x 7168 and leave long K unchanged.  The narrow tile (256 x 128,
+// 32 columns per epilogue warp) has half the bytes a stage and 7 stages.
 constexpr int kDenseStages = 5;
+constexpr int kDenseStagesNarrow = 7;
 constexpr int kDenseEpiWarps = 16;
 constexpr int kDenseBoxes = 1;
 constexpr int kDenseBoxW = 32;  // columns of a warp's C store box (32: 64-byte swizzle, 64: 128-byte)
 
-template <int MODE>
+template <int MODE, int BN>
 struct PairKernel {
-  using L = PairLayout<kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes, kDenseBoxW>;
-  static constexpr auto fn = dense_pair_kernel<MODE, kDenseBN, kDenseStages, kDenseEpiWarps, kDenseBoxes, kDenseBoxW>;
+  static constexpr int kStages = BN == kDenseBN ? kDenseStages : kDenseStagesNarrow;
+  using L = PairLayout<BN, kStages, kDenseEpiWarps, kDenseBoxes, kDenseBoxW>;
+  static constexpr auto fn = dense_pair_kernel<MODE, BN, kStages, kDenseEpiWarps, kDenseBoxes, kDenseBoxW>;
   static constexpr int kThreads = 64 + 32 * kDenseEpiWarps;
   static cudaError_t prepare() {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
   }
 };
+
+// Tile width of a dense launch: the one with the smaller estimate of waves of
+// pair tiles x tile width x cost of a column.  A narrow tile's column costs more
+// (each CTA stages its 128 rows of A once per 128 columns instead of per 256,
+// and every tile pays the pipeline's fill and the epilogue's drain).  The
+// narrow tile wins only where the wide one leaves pairs of SMs idle: a launch
+// with fewer 256-wide tiles than pairs.
+constexpr double kDenseNarrowColumnCost = 1.4;
+
+int dense_tile_bn(int64_t M, int64_t N, int num_sms, int pinned) {
+  if (pinned) return pinned;
+  const int64_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  const int64_t mp = (M + 2 * kBM - 1) / (2 * kBM);
+  const int64_t tiles_w = mp * ((N + kDenseBN - 1) / kDenseBN);
+  const int64_t tiles_n = mp * ((N + kDenseBNarrow - 1) / kDenseBNarrow);
+  const double est_w = static_cast<double>((tiles_w + pairs - 1) / pairs) * kDenseBN;
+  const double est_n =
+      static_cast<double>((tiles_n + pairs - 1) / pairs) * kDenseBNarrow * kDenseNarrowColumnCost;
+  return est_n < est_w ? kDenseBNarrow : kDenseBN;
+}
 
 // The gather-GEMM (ptpc, any K; the gathered workload's K is 512): 3 stages of
 // 48 KB (A 16 KB + the whole B tile 32 KB), 8 epilogue warps.
@@ -617,16 +649,16 @@ sg_status_t launch_error(cudaError_t e) {
   return SG_ERR_CUDA;
 }
 
-template <int MODE>
+template <int MODE, int BN>
 sg_status_t launch_dense_impl(const LaunchArgs& a) {
-  using Kern = PairKernel<MODE>;
+  using Kern = PairKernel<MODE, BN>;
   const bool bf16 = (MODE == kModeBf16);
   const int bk = dense_bk(MODE);
   const CUtensorMapDataType dt = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const uint64_t el = bf16 ? 2 : 1;
   CUtensorMap tmA, tmB, tmC;
   if (!encode_2d(&tmA, dt, a.A, a.K, a.M, a.K * el, bk, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, kDenseBN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmB, dt, a.B, a.K, a.N, a.K * el, bk, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_c(&tmC, a, kDenseBoxW))
     return SG_ERR_CUDA;
   GemmParams p{};
@@ -634,7 +666,7 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
   p.N = static_cast<int32_t>(a.N);
   p.K = static_cast<int32_t>(a.K);
   p.m_blocks = static_cast<int32_t>((a.M + kBM - 1) / kBM);
-  p.n_blocks = static_cast<int32_t>((a.N + kDenseBN - 1) / kDenseBN);
+  p.n_blocks = static_cast<int32_t>((a.N + BN - 1) / BN);
   p.k_blocks = static_cast<int32_t>((a.K + bk - 1) / bk);
   p.num_tiles = p.m_blocks * p.n_blocks;
   p.skip_kstep = a.skip_kstep;
@@ -645,31 +677,30 @@ sg_status_t launch_dense_impl(const LaunchArgs& a) {
   const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
   const int max_pairs = a.num_sms / 2;
   const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs, 1, 1);
-  cfg.blockDim = dim3(Kern::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Kern::L::kDynSmem;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return launch_error(cudaLaunchKernelEx(&cfg, Kern::fn, tmA, tmB, tmC, p));
+  GemmLaunch l(dim3(2 * pairs), dim3(Kern::kThreads), Kern::L::kDynSmem, a.stream, 2);
+  return launch_error(cudaLaunchKernelEx(&l.cfg, Kern::fn, tmA, tmB, tmC, p));
+}
+
+template <int MODE>
+sg_status_t launch_dense_mode(const LaunchArgs& a) {
+  return dense_tile_bn(a.M, a.N, a.num_sms, a.tile_bn) == kDenseBNarrow ? launch_dense_impl<MODE, kDenseBNarrow>(a)
+                                                                         : launch_dense_impl<MODE, kDenseBN>(a);
 }
 
 }  // namespace
 
 cudaError_t dense_prepare(int mode) {
-  if (mode == kModeBf16) return PairKernel<kModeBf16>::prepare();
-  const cudaError_t e = PairKernel<kModePtpc>::prepare();
+  if (mode == kModeBf16) {
+    const cudaError_t e = PairKernel<kModeBf16, kDenseBN>::prepare();
+    return e == cudaSuccess ? PairKernel<kModeBf16, kDenseBNarrow>::prepare() : e;
+  }
+  cudaError_t e = PairKernel<kModePtpc, kDenseBN>::prepare();
+  if (e == cudaSuccess) e = PairKernel<kModePtpc, kDenseBNarrow>::prepare();
   return e == cudaSuccess ? GatherKernel::prepare() : e;
 }
 
 sg_status_t dense_launch(const LaunchArgs& a) {
-  return a.mode == kModeBf16 ? launch_dense_impl<kModeBf16>(a) : launch_dense_impl<kModePtpc>(a);
+  return a.mode == kModeBf16 ? launch_dense_mode<kModeBf16>(a) : launch_dense_mode<kModePtpc>(a);
 }
 
 sg_status_t dense_launch_gather(const LaunchArgs& a) {
@@ -695,15 +726,18 @@ sg_status_t dense_launch_gather(const LaunchArgs& a) {
   p.gather_idx = a.gather_idx;
   p.rows_src = static_cast<int32_t>(a.rows_src);
   const int ctas = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
-  GatherKernel::fn<<<ctas, GatherKernel::kThreads, GatherKernel::L::kDynSmem, a.stream>>>(tmB, tmC, p);
-  return launch_error(cudaGetLastError());
+  GemmLaunch l(dim3(ctas), dim3(GatherKernel::kThreads), GatherKernel::L::kDynSmem, a.stream, 1);
+  return launch_error(cudaLaunchKernelEx(&l.cfg, GatherKernel::fn, tmB, tmC, p));
 }
 
-void dense_config(int mode, int64_t /*K*/, TileConfig* c) {
+bool dense_tile_ok(int bn) { return bn == kDenseBN || bn == kDenseBNarrow; }
+
+void dense_config(int mode, int64_t M, int64_t N, int num_sms, int tile_bn, TileConfig* c) {
+  const int bn = dense_tile_bn(M, N, num_sms, tile_bn);
   c->bm = kBM;
-  c->bn = kDenseBN;
+  c->bn = bn;
   c->bk = dense_bk(mode);
-  c->stages = kDenseStages;
+  c->stages = bn == kDenseBN ? kDenseStages : kDenseStagesNarrow;
   c->cluster = 2;  // pair MMA (cta_group::2) for every K
   c->rows_per_group = 2 * kBM;
 }

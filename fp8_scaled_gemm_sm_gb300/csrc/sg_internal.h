@@ -76,6 +76,37 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
 void note_cuda_error(cudaError_t e);
 const char* last_cuda_error();
 
+// Launch configuration of the GEMM kernels: `cluster` CTAs per cluster (1: no
+// cluster attribute) and programmatic stream serialization, so the launch may
+// begin while the previous kernel in the stream finishes; the kernels wait in
+// griddepcontrol.wait before touching global memory.  The attribute array lives
+// in the object: construct it in place and pass `cfg`.
+struct GemmLaunch {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2]{};
+  GemmLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, unsigned cluster) {
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster > 1) {
+      attr[n].id = cudaLaunchAttributeClusterDimension;
+      attr[n].val.clusterDim.x = cluster;
+      attr[n].val.clusterDim.y = 1;
+      attr[n].val.clusterDim.z = 1;
+      ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+  }
+  GemmLaunch(const GemmLaunch&) = delete;
+  GemmLaunch& operator=(const GemmLaunch&) = delete;
+};
+
 // cudaGetLastError after a launch, noted; SG_OK or SG_ERR_CUDA.
 inline sg_status_t launch_status() {
   const cudaError_t e = cudaGetLastError();
@@ -91,7 +122,8 @@ sg_status_t quantize_launch(int mode, bool bf16, const void* X, int64_t R, int64
 cudaError_t dense_prepare(int mode);
 sg_status_t dense_launch(const LaunchArgs& a);
 sg_status_t dense_launch_gather(const LaunchArgs& a);  // ptpc, A rows gathered by a.gather_idx
-void dense_config(int mode, int64_t K, TileConfig* c);
+void dense_config(int mode, int64_t M, int64_t N, int num_sms, int tile_bn, TileConfig* c);
+bool dense_tile_ok(int bn);  // a width scaled_gemm_set_tile may pin for ptpc / bf16
 
 cudaError_t mxfp8_prepare();
 size_t mxfp8_workspace_bytes(int64_t M_max, int64_t N, int64_t K);  // scale records

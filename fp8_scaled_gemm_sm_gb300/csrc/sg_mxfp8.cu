@@ -156,6 +156,8 @@ struct RecGeom {
 __global__ void __launch_bounds__(256)
     mx_scale_records_kernel(const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
                             uint32_t* __restrict__ rec_a, uint32_t* __restrict__ rec_b, RecGeom g) {
+  grid_dep_launch();
+  grid_dep_wait();  // the previous GEMM may still read the records this kernel rewrites
   const int64_t words_a = g.a_records() * 128;
   const int64_t words_b = g.b_rows() * 128;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < words_a + words_b;
@@ -287,6 +289,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = misc[0];
   const Watchdog wd{p.status, p.timeout_ns, reinterpret_cast<volatile int*>(&misc[1])};
+  grid_dep_launch();
+  grid_dep_wait();  // no global memory is touched before this point
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
@@ -500,19 +504,8 @@ sg_status_t launch_pair(const LaunchArgs& a, const RecGeom& g, const uint32_t* r
   const int pair_tiles = static_cast<int>((a.M + 2 * kBM - 1) / (2 * kBM)) * p.n_blocks;
   const int max_pairs = a.num_sms / 2;
   const int pairs = pair_tiles < max_pairs ? pair_tiles : max_pairs;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pairs * 2, 1, 1);
-  cfg.blockDim = dim3(kMxThreads, 1, 1);
-  cfg.dynamicSmemBytes = MxLayout<BN>::kDynSmem;
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, mxfp8_pair_kernel<BN>, tmA, tmB, tmRA, tmRB, tmC, p);
+  GemmLaunch l(dim3(pairs * 2), dim3(kMxThreads), MxLayout<BN>::kDynSmem, a.stream, 2);
+  const cudaError_t e = cudaLaunchKernelEx(&l.cfg, mxfp8_pair_kernel<BN>, tmA, tmB, tmRA, tmRB, tmC, p);
   if (e != cudaSuccess) {
     note_cuda_error(e);
     cudaGetLastError();  // clear the non-sticky launch error
@@ -552,10 +545,14 @@ sg_status_t mxfp8_launch(const LaunchArgs& a) {
     const int64_t words = (g.a_records() + g.b_rows()) * 128;
     const int64_t blocks = (words + 255) / 256;
     const int grid = static_cast<int>(blocks < 4L * a.num_sms * 8 ? blocks : 4L * a.num_sms * 8);
-    mx_scale_records_kernel<<<grid, 256, 0, a.stream>>>(static_cast<const uint8_t*>(a.a_scale),
-                                                        static_cast<const uint8_t*>(a.b_scale), rec_a, rec_b, g);
-    const sg_status_t st = launch_status();
-    if (st != SG_OK) return st;
+    GemmLaunch l(dim3(grid), dim3(256), 0, a.stream, 1);
+    const cudaError_t e = cudaLaunchKernelEx(&l.cfg, mx_scale_records_kernel, static_cast<const uint8_t*>(a.a_scale),
+                                             static_cast<const uint8_t*>(a.b_scale), rec_a, rec_b, g);
+    if (e != cudaSuccess) {
+      note_cuda_error(e);
+      cudaGetLastError();  // clear the non-sticky launch error
+      return SG_ERR_CUDA;
+    }
   }
   return bn == kMxBN ? launch_pair<kMxBN>(a, g, rec_a, rec_b) : launch_pair<kMxBNarrow>(a, g, rec_a, rec_b);
 }

@@ -112,6 +112,24 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return true;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+//
+// The GEMM launches carry cudaLaunchAttributeProgrammaticStreamSerialization, so
+// a launch may start while the kernel before it in the stream is still running.
+// Every kernel lets the next one be scheduled as soon as it has set itself up
+// (grid_dep_launch: the next kernel is scheduled once every CTA of this grid has
+// issued it or exited) and, before its first global memory access, waits until
+// the kernel before it has completed and its memory operations are visible
+// (grid_dep_wait; at once when there is no such kernel).  Ordering in the stream
+// is therefore that of plain launches; what overlaps is the next kernel's
+// launch, barrier set-up and TMEM allocation with this kernel's last tiles.
+
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- proxy fences and named barriers -------------------------------------------
 
 // Orders this thread's generic-proxy shared-memory accesses before later
@@ -126,18 +144,8 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 2D tiled load of the box at (x = inner, y = outer) into shared memory; its bytes
-// complete the transaction count of `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// tma_load_2d with an L2 cache policy.
+// 2D tiled load of the box at (x = inner, y = outer) into this CTA's shared
+// memory with an L2 cache policy; its bytes complete the transaction count of `bar`.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
                                                  uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -404,16 +412,6 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -141,8 +141,8 @@ const char* scaled_gemm_status_string(sg_status_t s);
 /* Tile geometry of a launch at M = M_max: BM x BN output tiles per CTA (BN: the
  * tile's columns; CTA pairs share a BN-wide tile), BK elements of K per pipeline
  * stage, `stages` shared-memory stages, `grid` persistent CTAs (whole clusters,
- * where the kernel runs CTAs in pairs).  mxfp8 chooses BN per launch from M and N
- * (see scaled_gemm_set_tile), so a smaller M may use the other width.  Any output
+ * where the kernel runs CTAs in pairs).  mxfp8, ptpc and bf16 choose BN per launch
+ * from M and N (see scaled_gemm_set_tile), so a smaller M may use the other width.  Any output
  * pointer may be NULL.  Returns SG_ERR_INVALID_ARG for a NULL handle.
  * Cited: a review of ROCm/mori PR 809, Smaller points (the tile configuration a
  * kernel serves is validated and reported, and the default should follow the
@@ -155,8 +155,12 @@ sg_status_t scaled_gemm_get_config(sg_handle_t h, int* bm, int* bn, int* bk, int
  * Test section); a launch chooses 128 where 224-wide tiles would leave pairs of SMs
  * idle (small M), by an estimate of waves of tiles x width (the shape-aware default
  * a review of ROCm/mori PR 809, Smaller points, asks for).
- * The other modes have one width (256) and accept only 0 or that width.  Both
- * widths sum every output element over K in the same order of MMA instructions.
+ * ptpc and bf16 have two widths: 256 (256 x 256 tiles per CTA pair) and 128,
+ * chosen the same way (128 only where fewer 256-wide tiles than pairs of SMs
+ * exist, e.g. one row panel at M <= 256); the gather launch always uses its one
+ * 256-wide tile.  blockscale has one width (256) and accepts only 0 or 256.  The
+ * two widths of a mode sum every output element over K in the same order of MMA
+ * instructions, so they give the same bits.
  * Not to be called while a launch of the plan is being enqueued from another
  * thread.
  * Returns SG_ERR_INVALID_ARG for a NULL handle or a width the mode does not have. */

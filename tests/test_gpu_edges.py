@@ -6,13 +6,14 @@ every launch must pass the element-wise and relL2 bounds, be NaN-free, be
 bit-identical to the first and leave the guard tail intact (ROCm/mori PR 785,
 Test; ROCm/aiter PR 6539, Test Plan).
 
-* The pair kernel (ptpc and bf16) at one-row, ragged and tile-sized M against
-  N of 16, 48 and 144 columns: the odd CTA of a pair tile wholly past M, and a
-  CTA's half of B wholly past N (ROCm/mori PR 809, Worth a reviewer's
-  attention: the partial last column tile), at K of 5 and 9 stages.
+* The pair kernel (ptpc and bf16, 256- and 128-wide tiles) at one-row, ragged
+  and tile-sized M against N of 16, 48 and 144 columns: the odd CTA of a pair
+  tile wholly past M, and a CTA's half of B wholly past N (ROCm/mori PR 809,
+  Worth a reviewer's attention: the partial last column tile), at K of 5 and 9
+  blocks.
 * The short-K matrix: K of one to four 128-wide blocks (and one to eight
   64-wide bf16 blocks), including the tail-only K <= 256 where the K loop is
-  all tail (ROCm/mori PR 785, Problem), at N = 16, 144 and 6288.
+  all tail (ROCm/mori PR 785, Problem), at N = 16, 144 and 6288, both widths.
 * mxfp8 with e8m0 scale codes 0, 1, 127, 253 and 254 mixed per K block (ROCm/mori
   PR 785, cost table and Scope: the mode's power-of-two block scales).
 * blockscale with fp32 scales spread over 2^-40 .. 2^40, some of them zero.
@@ -38,11 +39,13 @@ def gpu():
     return gpu_util
 
 
-def _run(gpu, case, launches=8):
+def _run(gpu, case, launches=8, tile_bn=0):
     _, ref = oracle.gemm(case.mode, *case.numpy(), want_r=False)
     dc = gpu.DeviceCase(case)
     h = gpu.make_plan(case)
     try:
+        if tile_bn:
+            gpu.binding.scaled_gemm_set_tile(h, tile_bn)
         first = None
         for i in range(launches):
             dc.poison()
@@ -63,21 +66,25 @@ def _run(gpu, case, launches=8):
     return first, ref
 
 
+# these shapes have fewer 256-wide tiles than pairs of SMs, so a launch left to
+# choose takes the 128-wide tile: both widths are pinned in turn
+@pytest.mark.parametrize("tile", [128, 256])
 @pytest.mark.parametrize("mode", ["ptpc", "bf16"])
 @pytest.mark.parametrize("K", [640, 1152])
 @pytest.mark.parametrize("N", [16, 48, 144])
 @pytest.mark.parametrize("M", [1, 127, 129])
-def test_pair_kernel_edges(gpu, mode, M, N, K):
+def test_pair_kernel_edges(gpu, mode, M, N, K, tile):
     b_std = 0.02 if mode == "ptpc" else 1.0
-    _run(gpu, synth.make_case(mode, M, N, K, seed=M * 7 + N + K, b_std=b_std))
+    _run(gpu, synth.make_case(mode, M, N, K, seed=M * 7 + N + K, b_std=b_std), tile_bn=tile)
 
 
+@pytest.mark.parametrize("tile", [128, 256])
 @pytest.mark.parametrize("mode", ["ptpc", "bf16"])
 @pytest.mark.parametrize("N", [16, 144, 6288])
 @pytest.mark.parametrize("K", [32, 64, 128, 256, 384, 512])
-def test_short_k_matrix(gpu, mode, K, N):
+def test_short_k_matrix(gpu, mode, K, N, tile):
     b_std = 0.02 if mode == "ptpc" else 1.0
-    _run(gpu, synth.make_case(mode, 129, N, K, seed=K + N, b_std=b_std))
+    _run(gpu, synth.make_case(mode, 129, N, K, seed=K + N, b_std=b_std), tile_bn=tile)
 
 
 @pytest.mark.parametrize("M,N,K,tile", [(256, 448, 1024, 224), (300, 672, 2080, 224), (256, 448, 1024, 128),

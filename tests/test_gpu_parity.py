@@ -165,6 +165,48 @@ def test_mxfp8_narrow_tiles(gpu, M, N, K):
     _run_full(gpu, synth.make_case("mxfp8", M, N, K, seed=M + K + 1, b_std=0.02), launches=8, tile_bn=128)
 
 
+@pytest.mark.parametrize(
+    "mode,M,N,K",
+    [
+        ("ptpc", 1, 16, 16),        # smallest legal problem
+        ("ptpc", 129, 144, 1152),   # ragged M and N, 9 K blocks
+        ("ptpc", 300, 528, 416),    # several tiles, ragged K, half-tile N tail (528 = 4 x 128 + 16)
+        ("ptpc", 2304, 1280, 384),  # 90 pair tiles on 76 pairs: second tiles, both accumulators
+        ("bf16", 200, 448, 1024),   # ragged M, 3.5 tiles of 128 columns
+        ("bf16", 513, 1168, 320),   # partial last tile, ragged bf16 K (5 blocks of 64)
+    ],
+)
+def test_dense_narrow_tiles(gpu, mode, M, N, K):
+    # 256 x 128 pair tiles: B staged 64 rows per CTA, 32 columns per epilogue
+    # warp, 7 stages; the MMAs sum each output element over K in the same order
+    # as on the 256-wide tile, so the two widths agree bit for bit
+    case = synth.make_case(mode, M, N, K, seed=M + N + K, b_std=0.02 if mode == "ptpc" else 1.0)
+    narrow, _ = _run_full(gpu, case, launches=8, tile_bn=128)
+    wide, _ = _run_full(gpu, case, launches=2, tile_bn=256)
+    assert np.array_equal(narrow, wide)
+
+
+def test_dense_tile_width_follows_m(gpu):
+    # 128-wide where 256-wide tiles would not fill the pairs of SMs (one pair row
+    # of 28 tiles at M = 256), 256-wide otherwise; set_tile pins or restores
+    b = gpu.binding
+    small = b.scaled_gemm_create("ptpc", 7168, 7168, 256)
+    large = b.scaled_gemm_create("ptpc", 7168, 7168, 4096)
+    bf = b.scaled_gemm_create("bf16", 896, 1024, 4096)
+    try:
+        assert b.scaled_gemm_get_config(small)["bn"] == 128
+        assert b.scaled_gemm_get_config(small)["stages"] == 7
+        assert b.scaled_gemm_get_config(large)["bn"] == 256
+        assert b.scaled_gemm_get_config(bf)["bn"] == 256  # 64 wide tiles: one wave either way
+        b.scaled_gemm_set_tile(large, 128)
+        assert b.scaled_gemm_get_config(large)["bn"] == 128
+        b.scaled_gemm_set_tile(large, 0)
+        assert b.scaled_gemm_get_config(large)["bn"] == 256
+    finally:
+        for h in (small, large, bf):
+            b.scaled_gemm_destroy(h)
+
+
 def test_mxfp8_tile_width_follows_m(gpu):
     # a plan reports the width of a launch at M_max: 128 where 224-wide tiles would
     # leave pairs of SMs idle, 224 otherwise; set_tile pins a width or restores the choice
@@ -181,7 +223,8 @@ def test_mxfp8_tile_width_follows_m(gpu):
         assert b.scaled_gemm_get_config(large)["bn"] == 224
         L = b.lib()
         assert L.scaled_gemm_set_tile(large, 256) == 1 and L.scaled_gemm_set_tile(large, 96) == 1
-        assert L.scaled_gemm_set_tile(dense, 128) == 1 and L.scaled_gemm_set_tile(dense, 256) == 0
+        assert L.scaled_gemm_set_tile(dense, 224) == 1 and L.scaled_gemm_set_tile(dense, 96) == 1
+        assert L.scaled_gemm_set_tile(dense, 128) == 0 and L.scaled_gemm_set_tile(dense, 256) == 0
     finally:
         for h in (small, large, dense):
             b.scaled_gemm_destroy(h)
