@@ -55,6 +55,13 @@
  * workspace-free plan: the block-scaled MMA reads its scales from tensor memory in
  * a layout the K-block-major scale arrays do not have.)  Destroying a handle must
  * not race a launch on it.
+ *
+ * Every kernel is launched with programmatic stream serialization: it may be
+ * scheduled while the kernel before it on `stream` is still running, sets up its
+ * barriers and tensor memory, and then waits (griddepcontrol.wait) until that kernel
+ * has completed and its memory writes are visible before it reads or writes any
+ * global memory.  Launches on one stream therefore see each other's results exactly
+ * as plain stream-ordered launches do; only the set-up overlaps.
  */
 #ifndef SCALED_GEMM_H
 #define SCALED_GEMM_H
