@@ -22,7 +22,9 @@ from checker import check
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 528, 416), (129, 144, 1152)])
+# the first three shapes take the 128-wide tile (fewer 256-wide tiles than pairs
+# of SMs), the last one the 256-wide tile (128 of them)
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (300, 528, 416), (129, 144, 1152), (4096, 2048, 512)])
 def test_noalloc_matches_oracle_and_handle_launch(M, N, K):
     if not torch.cuda.is_available():
         pytest.fail("a GPU test ran without a GPU")
