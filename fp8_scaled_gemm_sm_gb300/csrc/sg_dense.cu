@@ -80,8 +80,6 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
   constexpr int kBK = (MODE == kModeBf16) ? 64 : 128;
   constexpr int kUmmaK = (MODE == kModeBf16) ? 16 : 32;
   constexpr int kKSteps = kBK / kUmmaK;
-  constexpr uint32_t kIdesc =
-      (MODE == kModeBf16) ? instr_desc(1, 1, 2 * kBM, BN) : instr_desc(0, 0, 2 * kBM, BN);
   constexpr uint32_t kTxPair = 2 * (L::kAStage + L::kBStage);  // both CTAs' bytes
   constexpr uint32_t kTmemCols = 512;
   constexpr int kAccStride = 256;
@@ -117,6 +115,15 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
     c.nb = tp - mp * p.n_blocks;
     c.mb = 2 * mp + rank;  // this CTA's 128-row block
     return c;
+  };
+  // Columns the MMAs of a tile in N block nb compute: BN, except in a ragged last
+  // block, where the remaining columns rounded up to 32 (a pair MMA's N is a
+  // multiple of 32) are enough.  Each CTA then stages the first tile_n / 2 rows of
+  // its half of B; the accumulator columns past tile_n are not written by the tile's
+  // MMAs and lie past N, where the stores are clipped.
+  auto tile_n = [&](int nb) {
+    const int rem = p.N - nb * BN;
+    return rem >= BN ? BN : ((rem + 31) & ~31);
   };
 
   if (threadIdx.x == 0) {
@@ -160,6 +167,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       bool ok = true;
       for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
         const TileCoord tc = coord(tp);
+        const int bhalf = tile_n(tc.nb) / 2;  // B rows this CTA gives the tile's MMAs
         for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
           if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
             ok = false;
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             const uint32_t fb = map_to_cta(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxPair);
             tma_load_2d_pair_hint(sA + stage * L::kAStage, &tmA, kb * kBK, tc.mb * kBM, fb, drop_a);
-            tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN + rank * (BN / 2), fb,
+            tma_load_2d_pair_hint(sB + stage * L::kBStage, &tmB, kb * kBK, tc.nb * BN + rank * bhalf, fb,
                                   keep_b);
             issued |= 1u << stage;
             last_par[stage] = phase;
@@ -206,6 +214,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
       for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs, ++it) {
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
+        const int ntile = tile_n(coord(tp).nb);
+        const uint32_t idesc = (MODE == kModeBf16) ? instr_desc(1, 1, 2 * kBM, ntile) : instr_desc(0, 0, 2 * kBM, ntile);
         if (!mbar_wait_cluster(tempty_bar(acc), acc_par ^ 1, wd, kWhereMmaTmemEmpty)) {
           ok = false;
           break;
@@ -225,9 +235,9 @@ __global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
             const uint64_t ad = desc_advance(da, k * kUmmaK * (kRowBytes / kBK));
             const uint64_t bd = desc_advance(db, k * kUmmaK * (kRowBytes / kBK));
             if constexpr (MODE == kModeBf16)
-              mma_f16_pair(d, ad, bd, kIdesc, (kb | k) != 0);
+              mma_f16_pair(d, ad, bd, idesc, (kb | k) != 0);
             else
-              mma_f8f6f4_pair(d, ad, bd, kIdesc, (kb | k) != 0);
+              mma_f8f6f4_pair(d, ad, bd, idesc, (kb | k) != 0);
           }
           mma_commit_pair_both(empty_bar(stage));
           if (++stage == STAGES) {
