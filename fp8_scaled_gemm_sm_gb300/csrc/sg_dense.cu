@@ -5,7 +5,9 @@
 //
 // Every K runs on CTA pairs (a cluster of two CTAs on neighbouring SMs), each
 // pair persistent over 256 x BN output tiles computed with the pair MMA
-// (tcgen05.mma.cta_group::2).  Per CTA:
+// (tcgen05.mma.cta_group::2); BN is 256, or 128 for launches with fewer 256-wide
+// tiles than pairs of SMs, and a ragged last N block runs its MMAs only as wide as
+// its remaining columns.  Per CTA:
 //   warp 0      TMA producer: waits empty[s], loads this CTA's A rows [128 x
 //               128 B] and its half of the tile's B rows [BN/2 x 128 B] (128-byte
 //               swizzle) into stage s; the bytes of both CTAs complete the even
@@ -33,7 +35,9 @@
 // UMMA commits").  The epilogue's generic shared-memory writes are fenced into
 // the async proxy by every writing thread before the TMA store is issued
 // (deepseek-ai/DeepGEMM PR 453, Fix).  No TMA load here is multicast: every
-// CTA loads its own operand rows from this GPU's memory.
+// CTA loads its own operand rows from this GPU's memory.  Each kernel touches
+// global memory only after griddepcontrol.wait (programmatic dependent launch:
+// the launch may begin while the previous kernel in the stream finishes).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
