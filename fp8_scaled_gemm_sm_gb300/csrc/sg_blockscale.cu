@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
         const TileCoord tc = coord(tp);
         for (int kb = 0; kb < p.k_blocks; ++kb, ++kstep) {
-          if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
+          if (!mbar_wait_cluster<true>(empty_bar(stage), phase ^ 1, wd, kWhereProducerEmpty)) {
             ok = false;
             break;
           }
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       uint32_t tpar = 0;
       for (int tp = pair; tp < num_pair_tiles; tp += npairs) {
         const TileCoord tc = coord(tp);
-        if (!mbar_wait(cstaged_bar, tpar, wd, kWhereEpiTmemFull)) break;
+        if (!mbar_wait<true>(cstaged_bar, tpar, wd, kWhereEpiTmemFull)) break;
         tpar ^= 1;
 #pragma unroll 1
         for (int ew = 0; ew < kBsWarps; ++ew) {
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       const uint64_t desc_a = kmajor_sw128_desc(sA), desc_b = kmajor_sw128_desc(sB);
       for (int tp = pair; tp < num_pair_tiles && ok; tp += npairs) {
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait_cluster(pempty_bar(part), ppar ^ 1, wd, kWhereMmaTmemEmpty) ||
-              !mbar_wait_cluster(full_bar(stage), phase, wd, kWhereMmaFull)) {
+          if (!mbar_wait_cluster<true>(pempty_bar(part), ppar ^ 1, wd, kWhereMmaTmemEmpty) ||
+              !mbar_wait_cluster<true>(full_bar(stage), phase, wd, kWhereMmaFull)) {
             ok = false;
             break;
           }
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
               if (kb + kScaleAhead == kblocks) tile_scale_ptrs(tn);
               load_scales(kb + kScaleAhead - kblocks, ring_a[d], ring_b[d]);
             }
-            ok = mbar_wait_cluster(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
+            ok = mbar_wait_cluster<true>(pfull_bar(part), ppar, wd, kWhereEpiTmemFull);
             if (!__all_sync(0xffffffffu, ok)) {
               ok = false;
               break;
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           if (d < kblocks) load_scales(d, ring_a[d], ring_b[d]);
       }
       // the strip's boxes were last read by the previous tile's stores
-      ok = mbar_wait(cfree_bar, cpar, wd, kWhereEpiTmemFull);
+      ok = mbar_wait<true>(cfree_bar, cpar, wd, kWhereEpiTmemFull);
       cpar ^= 1;
       if (!__all_sync(0xffffffffu, ok)) break;
 #pragma unroll
