@@ -12,7 +12,8 @@ start visible if it happened:
 * read after write: a bf16 GEMM whose A is the output of the GEMM launched just
   before it (that output NaN-poisoned beforehand);
 * write after read: a GEMM whose output overwrites the A operand of the GEMM
-  launched just before it;
+  launched just before it (ptpc, blockscale, mxfp8), or the source cache of a
+  gather-GEMM;
 * one mxfp8 plan launched twice in a row with different scales: the second
   launch's scale-record kernel rewrites the workspace the first launch's GEMM reads.
 """
@@ -79,11 +80,13 @@ def test_gemm_reads_the_output_of_the_gemm_before_it(b):
         b.scaled_gemm_destroy(h2)
 
 
-def test_gemm_output_overwrites_the_input_of_the_gemm_before_it(b):
-    # C1 = ptpc(A1, B1) runs first; the next launch (bf16) writes its output over
-    # A1's bytes.  C1 must match the oracle on the original A1.
+@pytest.mark.parametrize("mode", ["ptpc", "blockscale", "mxfp8"])
+def test_gemm_output_overwrites_the_input_of_the_gemm_before_it(b, mode):
+    # C1 = op(A1, B1) runs first (mxfp8: its scale-record kernel, then the GEMM);
+    # the next launch (bf16) writes its output over A1's bytes.  C1 must match the
+    # oracle on the original A1.
     M, N1, K1 = 4096, 1024, 4096
-    c1 = synth.make_case("ptpc", M, N1, K1, seed=21, b_std=0.02)
+    c1 = synth.make_case(mode, M, N1, K1, seed=21, b_std=0.02)
     dev = torch.device("cuda")
     A1, B1, sa1, sb1 = c1.A.to(dev), c1.B.to(dev), c1.sa.to(dev), c1.sb.to(dev)
     # bf16 GEMM whose output [M2, N2] covers A1's M x K1 bytes exactly
@@ -91,9 +94,9 @@ def test_gemm_output_overwrites_the_input_of_the_gemm_before_it(b):
     c2 = synth.make_case("bf16", M2, N2, K2, seed=22)
     A2, B2 = c2.A.to(dev), c2.B.to(dev)
     C1 = torch.empty((M, N1), dtype=torch.int16, device=dev)
-    h1 = b.scaled_gemm_create("ptpc", N1, K1, M)
+    h1 = b.scaled_gemm_create(mode, N1, K1, M)
     h2 = b.scaled_gemm_create("bf16", N2, K2, M2)
-    _, ref1 = oracle.gemm("ptpc", *c1.numpy(), want_r=False)
+    _, ref1 = oracle.gemm(mode, *c1.numpy(), want_r=False)
     _, ref2 = oracle.gemm("bf16", *c2.numpy(), want_r=False)
     try:
         for rep in range(3):
@@ -106,6 +109,39 @@ def test_gemm_output_overwrites_the_input_of_the_gemm_before_it(b):
             r = check(C1.cpu().numpy().view(np.uint16), ref1)
             assert r["ok"], (rep, r)
             r = check(A1.view(torch.int16).cpu().numpy().view(np.uint16).reshape(M2, N2), ref2)
+            assert r["ok"], (rep, r)
+        for h in (h1, h2):
+            assert b.scaled_gemm_debug_status(h)[0] == 0
+    finally:
+        b.scaled_gemm_destroy(h1)
+        b.scaled_gemm_destroy(h2)
+
+
+def test_gather_gemm_source_overwritten_by_the_next_launch(b):
+    # the gather-GEMM reads its A rows with cp.async from the source cache; the next
+    # launch (bf16) overwrites that cache.  The gathered result must be the oracle's
+    # on the original cache.
+    M, R, N, K = 4096, 8192, 1024, 2048
+    g = synth.make_gather_case(M, R, N, K, seed=41, page=16)
+    dev = torch.device("cuda")
+    A_src, idx, B, sa, sb = (t.to(dev) for t in (g.A_src, g.idx, g.B, g.sa_src, g.sb))
+    M2, N2, K2 = R, K // 2, 256  # bf16 output [R, K/2] covers the R x K source bytes
+    c2 = synth.make_case("bf16", M2, N2, K2, seed=42)
+    A2, B2 = c2.A.to(dev), c2.B.to(dev)
+    C = torch.empty((M, N), dtype=torch.int16, device=dev)
+    _, ref = oracle.gemm_gather(*g.numpy(), want_r=False)
+    h1 = b.scaled_gemm_create("ptpc", N, K, M)
+    h2 = b.scaled_gemm_create("bf16", N2, K2, M2)
+    try:
+        for rep in range(3):
+            A_src.copy_(g.A_src.to(dev))
+            C.fill_(NAN_BF16)
+            s = torch.cuda.current_stream().cuda_stream
+            b.scaled_gemm_launch_gather(h1, A_src.data_ptr(), R, idx.data_ptr(), B.data_ptr(), sa.data_ptr(),
+                                        sb.data_ptr(), C.data_ptr(), M, s)
+            b.scaled_gemm_launch(h2, A2.data_ptr(), B2.data_ptr(), 0, 0, A_src.data_ptr(), M2, s)
+            torch.cuda.synchronize()
+            r = check(C.cpu().numpy().view(np.uint16), ref)
             assert r["ok"], (rep, r)
         for h in (h1, h2):
             assert b.scaled_gemm_debug_status(h)[0] == 0
