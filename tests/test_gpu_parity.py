@@ -207,6 +207,31 @@ def test_dense_tile_width_follows_m(gpu):
             b.scaled_gemm_destroy(h)
 
 
+def test_dense_plan_switches_width_between_launches(gpu):
+    # one plan launched back to back with an M that takes the 128-wide tile (256
+    # rows: 8 wide tiles for 76 pairs) and one that takes the 256-wide tile (4096
+    # rows): every launch matches the oracle on its rows and leaves the rows past
+    # its M untouched
+    case = synth.make_case("ptpc", 4096, 2048, 512, seed=51, b_std=0.02)
+    _, ref = oracle.gemm("ptpc", *case.numpy(), want_r=False)
+    dc = gpu.DeviceCase(case)
+    h = gpu.make_plan(case)
+    try:
+        for M in (256, 4096, 256, 4096):
+            dc.poison()
+            dc.launch(h, M=M)
+            torch.cuda.synchronize()
+            bits = dc.c_bits()
+            r = check(bits[:M], ref[:M])
+            assert r["ok"], (M, r)
+            assert (bits[M:] == gpu.NAN_BF16).all(), "rows past M were written (M = %d)" % M
+            assert dc.canary_ok()
+        code, where = gpu.binding.scaled_gemm_debug_status(h)
+        assert code == 0, (code, where)
+    finally:
+        gpu.binding.scaled_gemm_destroy(h)
+
+
 def test_mxfp8_tile_width_follows_m(gpu):
     # a plan reports the width of a launch at M_max: 128 where 224-wide tiles would
     # leave pairs of SMs idle, 224 otherwise; set_tile pins a width or restores the choice
