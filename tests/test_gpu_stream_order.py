@@ -15,7 +15,9 @@ start visible if it happened:
   launched just before it (ptpc, blockscale, mxfp8), or the source cache of a
   gather-GEMM;
 * one mxfp8 plan launched twice in a row with different scales: the second
-  launch's scale-record kernel rewrites the workspace the first launch's GEMM reads.
+  launch's scale-record kernel rewrites the workspace the first launch's GEMM reads;
+* every kernel of the path (ptpc, bf16, blockscale, mxfp8, gather) chained ten
+  times over in one CUDA graph, replayed twice.
 """
 import numpy as np
 import pytest
@@ -175,3 +177,71 @@ def test_mxfp8_plan_launched_twice_in_a_row(b):
         assert b.scaled_gemm_debug_status(h)[0] == 0
     finally:
         b.scaled_gemm_destroy(h)
+
+
+def test_every_kernel_chained_in_a_cuda_graph(b):
+    # ptpc, bf16, blockscale, mxfp8 (scale records + GEMM) and the gather-GEMM
+    # launched in turn, 10 rounds, captured in one CUDA graph: every kernel
+    # boundary of the path appears as a programmatic dependency in the graph.
+    # After two replays every output matches the oracle and is bit-identical to
+    # the first replay's.
+    dev = torch.device("cuda")
+    M, N, K = 512, 1024, 1024
+    jobs = []
+    for i, mode in enumerate(("ptpc", "bf16", "blockscale", "mxfp8")):
+        c = synth.make_case(mode, M, N, K, seed=61 + i, b_std=0.02 if mode != "bf16" else 1.0)
+        ops = [c.A.to(dev), c.B.to(dev)] + ([] if mode == "bf16" else [c.sa.to(dev), c.sb.to(dev)])
+        C = torch.empty((M, N), dtype=torch.int16, device=dev)
+        ref = oracle.gemm(mode, *c.numpy(), want_r=False)[1]
+        jobs.append((mode, b.scaled_gemm_create(mode, N, K, M), ops, C, ref))
+    g = synth.make_gather_case(M, 2048, N, K, seed=65, page=16)
+    gops = [t.to(dev) for t in (g.A_src, g.idx, g.B, g.sa_src, g.sb)]
+    gC = torch.empty((M, N), dtype=torch.int16, device=dev)
+    gref = oracle.gemm_gather(*g.numpy(), want_r=False)[1]
+    gh = b.scaled_gemm_create("ptpc", N, K, M)
+    stream = torch.cuda.Stream()
+    try:
+        def launch_all():
+            s = stream.cuda_stream
+            for mode, h, ops, C, _ in jobs:
+                sa = ops[2].data_ptr() if len(ops) > 2 else 0
+                sb = ops[3].data_ptr() if len(ops) > 2 else 0
+                b.scaled_gemm_launch(h, ops[0].data_ptr(), ops[1].data_ptr(), sa, sb, C.data_ptr(), M, s)
+            A_src, idx, B, sa_src, sb = gops
+            b.scaled_gemm_launch_gather(gh, A_src.data_ptr(), 2048, idx.data_ptr(), B.data_ptr(), sa_src.data_ptr(),
+                                        sb.data_ptr(), gC.data_ptr(), M, s)
+
+        with torch.cuda.stream(stream):
+            launch_all()  # first use sets the plans' kernels up outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(10):
+                launch_all()
+        first = None
+        for rep in range(2):
+            for _, _, _, C, _ in jobs:
+                C.fill_(NAN_BF16)
+            gC.fill_(NAN_BF16)
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            outs = [C.cpu().numpy().view(np.uint16) for _, _, _, C, _ in jobs] + [gC.cpu().numpy().view(np.uint16)]
+            refs = [ref for *_, ref in jobs] + [gref]
+            names = [mode for mode, *_ in jobs] + ["gather"]
+            for name, out, ref in zip(names, outs, refs):
+                r = check(out, ref)
+                assert r["ok"], (rep, name, r)
+            if first is None:
+                first = outs
+            else:
+                for name, a, c in zip(names, first, outs):
+                    assert np.array_equal(a, c), name
+        del graph
+        for _, h, _, _, _ in jobs:
+            assert b.scaled_gemm_debug_status(h)[0] == 0
+        assert b.scaled_gemm_debug_status(gh)[0] == 0
+    finally:
+        for _, h, _, _, _ in jobs:
+            b.scaled_gemm_destroy(h)
+        b.scaled_gemm_destroy(gh)
