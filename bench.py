@@ -436,24 +436,28 @@ def run_gpu(args, control, rank, local):
             peak_kind, "" if peak_kind_run == "burst" else "_sustained", peak_kind_run, peak_why),
     }
 
-    # bad launches: 20 launches per workload into NaN-poisoned outputs, each
-    # bit-identical to the first and NaN-free (parity against the oracle is in tests/)
+    # bad launches: 20 launches per workload into NaN-poisoned outputs followed by
+    # a guard tail, each bit-identical to the first, NaN-free and leaving the tail
+    # untouched (parity against the oracle is in tests/)
     bad = 0
     with torch.cuda.stream(stream):
         for d in ([] if args.no_bad_check else work):
+            c = d["case"]
+            buf = torch.empty(c.M * c.N + 4096, dtype=torch.int16, device=dev)
+            Cg, tail = buf[: c.M * c.N].view(c.M, c.N), buf[c.M * c.N:]
+            tail.fill_(0x5A5A)
             first = None
             for _ in range(20):
-                d["C"].view(torch.int16).fill_(0x7FC0)
-                launch(d)
-                cur = d["C"].view(torch.int16)
-                isnan = torch.isnan(d["C"]).any()
+                Cg.fill_(0x7FC0)
+                launch(d, Cg.view(torch.bfloat16))
+                isnan = torch.isnan(Cg.view(torch.bfloat16)).any()
+                ok = (not bool(isnan)) and bool((tail == 0x5A5A).all())
                 if first is None:
-                    first = cur.clone()
-                    ok = not bool(isnan)
+                    first = Cg.clone()
                 else:
-                    ok = (not bool(isnan)) and torch.equal(cur, first)
+                    ok = ok and torch.equal(Cg, first)
                 bad += 0 if ok else 1
-            del first
+            del first, buf
     torch.cuda.synchronize()
     status_bad = 0
     for d in work:
@@ -503,6 +507,7 @@ def run_gpu(args, control, rank, local):
         "clocks": clk,
         "gpu_launches": args.steps * sum(KERNELS_PER_LAUNCH.get(d["case"].mode, 1) for d in work),
         "bad_launches": {"per_workload": 0 if args.no_bad_check else 20, "workloads": n, "bad": bad,
+                         "checks": "NaN-free, bit-identical to the first launch, 4096-element guard tail untouched",
                          "watchdog_timeouts": status_bad},
         "per_config": per,
         "wall_s_timed": round(wall1 - wall0, 4),
